@@ -1,0 +1,361 @@
+// C-ABI front end of libsk: argument validation (before any CUDA call), the
+// device check, TMA descriptor encoding, split-count choice and kernel chaining.
+// Validation mirrors the unpooler page's Unpooler.unsupported, Unpooler.run and
+// launch_unsupported: shape, dtype (here: the caller's contract), contiguity
+// and 16-byte alignment are checked before launch and reported as a reason
+// string.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "sk.h"
+#include "sk_internal.h"
+
+namespace {
+
+thread_local std::string t_last_error;
+
+sk_status fail(sk_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+sk_status ok() {
+  t_last_error.clear();
+  return SK_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char *v = std::getenv("SK_NO_PDL");
+    return !(v && v[0] && v[0] != '0');
+  }();
+  return on;
+}
+
+// Current device, checked to be compute capability 10.3, with its one-time
+// set-up done.
+sk_status current_device(sk::DeviceInfo *info) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(SK_ERR_CUDA, "no usable CUDA device: %s", cudaGetErrorString(e));
+  if (std::getenv("SK_FORCE_ARCH_FAIL"))
+    return fail(SK_ERR_ARCH, "device %d rejected (SK_FORCE_ARCH_FAIL is set)", dev);
+  e = sk::device_setup(dev, info);
+  if (e != cudaSuccess)
+    return fail(SK_ERR_CUDA, "device %d set-up failed: %s", dev, cudaGetErrorString(e));
+  if (info->major != 10 || info->minor != 3)
+    return fail(SK_ERR_ARCH, "libsk needs a compute capability 10.3 GPU (GB300); device %d is %d.%d",
+                dev, info->major, info->minor);
+  return SK_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D BF16 tensor map over a row-major [rows, cols] matrix, box
+// [box_rows, 64 columns], 128-byte swizzle (the layout the MMA descriptors
+// expect). Rows past `rows` read as zero.
+sk_status make_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(sk::kBlockK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return SK_OK;
+}
+
+sk_status check_gemm_shape(int m, int n, int k, int splits) {
+  if (m < 1 || m > SK_MAX_M)
+    return fail(SK_ERR_INVALID_ARG, "m=%d: needs 1 <= m <= %d token rows", m, SK_MAX_M);
+  if (n <= 0 || n % 16)
+    return fail(SK_ERR_INVALID_ARG, "n=%d: needs a positive multiple of 16 output features", n);
+  if (k <= 0 || k % sk::kBlockK)
+    return fail(SK_ERR_INVALID_ARG, "k=%d: needs a positive multiple of %d", k, sk::kBlockK);
+  if (splits != 0 && splits != 1 && splits != 2 && splits != 4 && splits != 8 && splits != 16)
+    return fail(SK_ERR_UNSUPPORTED, "unsupported split count %d (0, 1, 2, 4, 8 or 16)", splits);
+  if (splits > 0 && k % (sk::kBlockK * splits))
+    return fail(SK_ERR_UNSUPPORTED, "K=%d does not split into %d slices of whole %d-wide blocks", k,
+                splits, sk::kBlockK);
+  return SK_OK;
+}
+
+// Automatic split count: the largest S in {1, 2, 4, 8, 16} that divides K into
+// whole 64-wide blocks while tiles x S stays within one CTA per SM. A single
+// row tile (small n) may use up to 16 ranks.
+int auto_splits(int n, int k, int sm_count) {
+  const int tiles = (n + sk::kTileN - 1) / sk::kTileN;
+  int best = 1;
+  for (int s = 2; s <= 16; s *= 2) {
+    if (k % (sk::kBlockK * s)) break;
+    if (tiles * s > sm_count) break;
+    best = s;
+  }
+  return best;
+}
+
+int choose_stages(int n, int k, int splits, int sm_count) {
+  const int nkb = k / (sk::kBlockK * splits);
+  const int tiles = (n + sk::kTileN - 1) / sk::kTileN;
+  int st = tiles * splits <= sm_count ? sk::kMaxStages : 5;  // 5 stages: two CTAs fit an SM
+  if (const char *v = std::getenv("SK_STAGES")) {
+    const int forced = std::atoi(v);
+    if (forced >= 1 && forced <= sk::kMaxStages) st = forced;
+  }
+  return st < nkb ? st : nkb;
+}
+
+cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+sk_status launch_status(cudaError_t e, const char *what) {
+  if (e != cudaSuccess) return fail(SK_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(e));
+  return ok();
+}
+
+// Validated GEMM enqueue shared by the three GEMM entry points.
+sk_status enqueue_gemm(const void *x, const void *w, void *y, int m, int n, int k, int splits,
+                       void *stream, const sk::DeviceInfo &info) {
+  const int s = splits ? splits : auto_splits(n, k, info.sm_count);
+  CUtensorMap tw, tx;
+  sk_status st;
+  if ((st = make_map(&tw, w, n, k, sk::kTileN)) != SK_OK) return st;
+  if ((st = make_map(&tx, x, m, k, sk::kTokTile)) != SK_OK) return st;
+  const int stages = choose_stages(n, k, s, info.sm_count);
+  return launch_status(sk::launch_gemm(tw, tx, static_cast<uint16_t *>(y), m, n, k, s, stages,
+                                       as_stream(stream), pdl_enabled()),
+                       "gemm");
+}
+
+sk_status check_ptrs16(const char *names, std::initializer_list<const void *> ps) {
+  int i = 0;
+  for (const void *p : ps) {
+    if (!p) return fail(SK_ERR_INVALID_ARG, "null pointer (argument %d of %s)", i, names);
+    if (!aligned16(p))
+      return fail(SK_ERR_INVALID_ARG, "pointer %p (argument %d of %s) is not 16-byte aligned", p, i,
+                  names);
+    ++i;
+  }
+  return SK_OK;
+}
+
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" {
+
+const char *sk_last_error(void) { return t_last_error.c_str(); }
+
+int sk_version(void) { return SK_VERSION; }
+
+sk_status sk_gemm_supported(int m, int n, int k, int splits) {
+  sk_status st = check_gemm_shape(m, n, k, splits);
+  return st == SK_OK ? ok() : st;
+}
+
+int sk_gemm_splits(int m, int n, int k, int splits) {
+  if (check_gemm_shape(m, n, k, splits) != SK_OK) return 0;
+  if (splits) return splits;
+  sk::DeviceInfo info;
+  if (current_device(&info) != SK_OK) return 0;
+  ok();
+  return auto_splits(n, k, info.sm_count);
+}
+
+sk_status sk_gemm_bf16(const void *x, const void *w, void *y, int m, int n, int k, int splits,
+                       void *stream) {
+  sk_status st;
+  if ((st = check_gemm_shape(m, n, k, splits)) != SK_OK) return st;
+  if ((st = check_ptrs16("sk_gemm_bf16(x, w, y)", {x, w, y})) != SK_OK) return st;
+  sk::DeviceInfo info;
+  if ((st = current_device(&info)) != SK_OK) return st;
+  return enqueue_gemm(x, w, y, m, n, k, splits, stream, info);
+}
+
+static sk_status check_norm_quant(int m, int n) {
+  if (m < 1 || m > SK_MAX_M)
+    return fail(SK_ERR_INVALID_ARG, "m=%d: needs 1 <= m <= %d token rows", m, SK_MAX_M);
+  if (n < 16 || n % 16 || n > 16384)
+    return fail(SK_ERR_INVALID_ARG, "n=%d: needs a multiple of 16 in [16, 16384]", n);
+  return SK_OK;
+}
+
+sk_status sk_rmsnorm_nvfp4(const void *y, const void *norm_w, float eps, float gain_center,
+                           const float *global_scale, uint8_t *a, uint8_t *a_sf, void *z_out,
+                           int m, int n, void *stream) {
+  sk_status st;
+  if ((st = check_norm_quant(m, n)) != SK_OK) return st;
+  if ((st = check_ptrs16("sk_rmsnorm_nvfp4(y, norm_w, a)", {y, norm_w, a})) != SK_OK) return st;
+  if (!global_scale || (reinterpret_cast<uintptr_t>(global_scale) & 3))
+    return fail(SK_ERR_INVALID_ARG, "global_scale must be a 4-byte aligned device FP32 [1]");
+  if (!a_sf) return fail(SK_ERR_INVALID_ARG, "a_sf is null");
+  if (z_out && !aligned16(z_out)) return fail(SK_ERR_INVALID_ARG, "z_out is not 16-byte aligned");
+  sk::DeviceInfo info;
+  if ((st = current_device(&info)) != SK_OK) return st;
+  return launch_status(
+      sk::launch_rmsnorm_nvfp4(static_cast<const uint16_t *>(y), static_cast<const uint16_t *>(norm_w),
+                               eps, gain_center, global_scale, a, a_sf,
+                               static_cast<uint16_t *>(z_out), m, n, as_stream(stream),
+                               pdl_enabled()),
+      "rmsnorm_nvfp4");
+}
+
+size_t sk_gemm_rmsnorm_nvfp4_workspace(int m, int n) {
+  if (m <= 0 || n <= 0) return 0;
+  return round256(static_cast<size_t>(m) * n * 2);
+}
+
+sk_status sk_gemm_rmsnorm_nvfp4(const void *x, const void *w, const void *norm_w, float eps,
+                                float gain_center, const float *global_scale, uint8_t *a,
+                                uint8_t *a_sf, void *z_out, void *workspace,
+                                size_t workspace_bytes, int m, int n, int k, int splits,
+                                void *stream) {
+  sk_status st;
+  if ((st = check_gemm_shape(m, n, k, splits)) != SK_OK) return st;
+  if ((st = check_norm_quant(m, n)) != SK_OK) return st;
+  if ((st = check_ptrs16("sk_gemm_rmsnorm_nvfp4(x, w, norm_w, a, workspace)",
+                         {x, w, norm_w, a, workspace})) != SK_OK)
+    return st;
+  if (!global_scale || (reinterpret_cast<uintptr_t>(global_scale) & 3))
+    return fail(SK_ERR_INVALID_ARG, "global_scale must be a 4-byte aligned device FP32 [1]");
+  if (!a_sf) return fail(SK_ERR_INVALID_ARG, "a_sf is null");
+  if (z_out && !aligned16(z_out)) return fail(SK_ERR_INVALID_ARG, "z_out is not 16-byte aligned");
+  if (workspace_bytes < sk_gemm_rmsnorm_nvfp4_workspace(m, n))
+    return fail(SK_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes,
+                sk_gemm_rmsnorm_nvfp4_workspace(m, n));
+  sk::DeviceInfo info;
+  if ((st = current_device(&info)) != SK_OK) return st;
+  if ((st = enqueue_gemm(x, w, workspace, m, n, k, splits, stream, info)) != SK_OK) return st;
+  return launch_status(
+      sk::launch_rmsnorm_nvfp4(static_cast<const uint16_t *>(workspace),
+                               static_cast<const uint16_t *>(norm_w), eps, gain_center,
+                               global_scale, a, a_sf, static_cast<uint16_t *>(z_out), m, n,
+                               as_stream(stream), pdl_enabled()),
+      "rmsnorm_nvfp4");
+}
+
+sk_status sk_nvfp4_quantize(const void *z, const float *global_scale, uint8_t *a, uint8_t *a_sf,
+                            int m, int n, void *stream) {
+  sk_status st;
+  if (m < 1 || m > 65535) return fail(SK_ERR_INVALID_ARG, "m=%d: needs 1 <= m <= 65535", m);
+  if (n < 16 || n % 16) return fail(SK_ERR_INVALID_ARG, "n=%d: needs a positive multiple of 16", n);
+  if ((st = check_ptrs16("sk_nvfp4_quantize(z, a)", {z, a})) != SK_OK) return st;
+  if (!global_scale || (reinterpret_cast<uintptr_t>(global_scale) & 3))
+    return fail(SK_ERR_INVALID_ARG, "global_scale must be a 4-byte aligned device FP32 [1]");
+  if (!a_sf) return fail(SK_ERR_INVALID_ARG, "a_sf is null");
+  sk::DeviceInfo info;
+  if ((st = current_device(&info)) != SK_OK) return st;
+  return launch_status(sk::launch_nvfp4_quantize(static_cast<const uint16_t *>(z), global_scale, a,
+                                                 a_sf, m, n, as_stream(stream), pdl_enabled()),
+                       "nvfp4_quantize");
+}
+
+static sk_status check_dual(const void *partial, const float *resid, const void *post_w,
+                            const void *beta, const void *pre_w, const void *out, int m, int h) {
+  if (m < 1 || m > SK_MAX_M)
+    return fail(SK_ERR_INVALID_ARG, "m=%d: needs 1 <= m <= %d token rows", m, SK_MAX_M);
+  if (h < 8 || h % 8 || h > 8192)
+    return fail(SK_ERR_INVALID_ARG, "h=%d: needs a multiple of 8 in [8, 8192]", h);
+  sk_status st = check_ptrs16("sk_dual_norm_residual(partial, resid, beta, pre_w, out)",
+                              {partial, resid, beta, pre_w, out});
+  if (st != SK_OK) return st;
+  if (post_w && !aligned16(post_w)) return fail(SK_ERR_INVALID_ARG, "post_w is not 16-byte aligned");
+  return SK_OK;
+}
+
+sk_status sk_dual_norm_residual(const void *partial, float *resid, const void *post_w, float alpha,
+                                const void *beta, const void *pre_w, void *out, float eps_post,
+                                float eps_pre, float gc_post, float gc_pre, int m, int h,
+                                void *stream) {
+  sk_status st;
+  if ((st = check_dual(partial, resid, post_w, beta, pre_w, out, m, h)) != SK_OK) return st;
+  sk::DeviceInfo info;
+  if ((st = current_device(&info)) != SK_OK) return st;
+  return launch_status(
+      sk::launch_dual_norm(static_cast<const uint16_t *>(partial), resid,
+                           static_cast<const uint16_t *>(post_w), alpha,
+                           static_cast<const uint16_t *>(beta), static_cast<const uint16_t *>(pre_w),
+                           static_cast<uint16_t *>(out), eps_post, eps_pre, gc_post, gc_pre, m, h,
+                           as_stream(stream), pdl_enabled()),
+      "dual_norm");
+}
+
+size_t sk_gemm_dual_norm_workspace(int m, int n) {
+  if (m <= 0 || n <= 0) return 0;
+  return round256(static_cast<size_t>(m) * n * 2);
+}
+
+sk_status sk_gemm_dual_norm(const void *x, const void *w, float *resid, const void *post_w,
+                            float alpha, const void *beta, const void *pre_w, void *out,
+                            float eps_post, float eps_pre, float gc_post, float gc_pre,
+                            void *workspace, size_t workspace_bytes, int m, int n, int k,
+                            int splits, void *stream) {
+  sk_status st;
+  if ((st = check_gemm_shape(m, n, k, splits)) != SK_OK) return st;
+  if ((st = check_dual(workspace, resid, post_w, beta, pre_w, out, m, n)) != SK_OK) return st;
+  if ((st = check_ptrs16("sk_gemm_dual_norm(x, w)", {x, w})) != SK_OK) return st;
+  if (workspace_bytes < sk_gemm_dual_norm_workspace(m, n))
+    return fail(SK_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes,
+                sk_gemm_dual_norm_workspace(m, n));
+  sk::DeviceInfo info;
+  if ((st = current_device(&info)) != SK_OK) return st;
+  if ((st = enqueue_gemm(x, w, workspace, m, n, k, splits, stream, info)) != SK_OK) return st;
+  return launch_status(
+      sk::launch_dual_norm(static_cast<const uint16_t *>(workspace), resid,
+                           static_cast<const uint16_t *>(post_w), alpha,
+                           static_cast<const uint16_t *>(beta), static_cast<const uint16_t *>(pre_w),
+                           static_cast<uint16_t *>(out), eps_post, eps_pre, gc_post, gc_pre, m, n,
+                           as_stream(stream), pdl_enabled()),
+      "dual_norm");
+}
+
+sk_status sk_device_status(uint32_t *out, int clear) {
+  if (!out) return fail(SK_ERR_INVALID_ARG, "out is null");
+  sk::DeviceInfo info;
+  sk_status st;
+  if ((st = current_device(&info)) != SK_OK) return st;
+  cudaError_t e = sk::read_device_status(out, clear != 0);
+  if (e != cudaSuccess) return fail(SK_ERR_CUDA, "device status read failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+sk_status sk_convert_probe(int kind, const void *in, void *out, int n, void *stream) {
+  if (kind < 0 || kind > 3) return fail(SK_ERR_INVALID_ARG, "kind=%d: needs 0..3", kind);
+  if (n < 0) return fail(SK_ERR_INVALID_ARG, "n=%d < 0", n);
+  if (n == 0) return ok();
+  if (!in || !out) return fail(SK_ERR_INVALID_ARG, "null pointer");
+  sk::DeviceInfo info;
+  sk_status st;
+  if ((st = current_device(&info)) != SK_OK) return st;
+  return launch_status(sk::launch_convert_probe(kind, in, out, n, as_stream(stream)), "convert_probe");
+}
+
+}  // extern "C"

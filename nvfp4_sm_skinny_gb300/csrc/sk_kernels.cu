@@ -1,0 +1,600 @@
+// Device code of libsk: the small-M skinny GEMM (TMA weight stream into a
+// shared-memory ring, tcgen05 MMA into TMEM, cluster split-K reduced in DSMEM
+// in a fixed order), the pre-expert RMSNorm + NVFP4 epilogue, the NVFP4
+// quantizer and the attention-boundary dual norm.
+//
+// What the kernels compute follows the vLLM API pages of the Muse Spark
+// specialized decode: cutedsl/gemm/unpooler (module docstring: the small-M
+// product, the fixed-order split-K sum, -0.0 published as +0.0),
+// cutedsl/moe/pooler_gather (module docstring: pre-expert norm and NVFP4
+// layout; nvfp4_compute_output_scale and the cvt helpers), and
+// cutedsl/oproj/batt (AttentionBoundary: the dual norm).
+#include <mutex>
+#include <type_traits>
+
+#include "sk.h"
+#include "sk_internal.h"
+#include "sk_ptx.cuh"
+
+namespace sk {
+
+// OR of SK_DEVICE_WAIT_* bits, set by kernels whose bounded waits ran out.
+__device__ uint32_t g_device_status;
+
+constexpr uint32_t kIdesc = idesc_bf16_f32(kTileN, kTokTile);
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s of wall time per wait
+constexpr int kGemmThreads = 128;                  // 4 warps = the 128 TMEM lanes
+
+struct GemmArgs {
+  uint16_t *y;   // [m, n] BF16 bits
+  int m, n;
+  int kb_per_split;  // kBlockK-wide K blocks per CTA
+  int stages;
+  int splits;
+};
+
+// Bounded wait that also gives up as soon as another role raised `abort`.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile uint32_t *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// One CTA = kTileN weight rows x one K slice of kb_per_split * 64 elements.
+// Warp 0 lane 0: TMA producer. Warp 1 lane 0: MMA issuer. Warp 2 owns the
+// TMEM allocation. All four warps run the epilogue (one TMEM lane per thread).
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int stages = args.stages;
+  uint8_t *s_w = smem;                                   // stages x 16 KiB (1024-aligned)
+  uint8_t *s_x = smem + stages * kStageWBytes;           // stages x 2 KiB (1024-aligned)
+  uint64_t *bars = reinterpret_cast<uint64_t *>(s_x + stages * kStageXBytes);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * stages + 1);
+  volatile uint32_t *abort_flag = tmem_slot + 1;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n0 = blockIdx.x * kTileN;
+  const int nkb = args.kb_per_split;
+  const int kb0 = blockIdx.y * nkb;
+
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + stages);
+  const uint32_t done_bar = smem_u32(bars + 2 * stages);
+
+  if (tid == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_map(&tmap_w);
+    tma_prefetch_map(&tmap_x);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), 32);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  // Dependents may be scheduled as soon as every CTA of this grid is resident;
+  // they order themselves after this grid with their own griddepcontrol.wait.
+  griddep_launch_dependents();
+
+  int issued = 0;
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------- TMA producer
+    const uint64_t pol_w = l2_policy_evict_first();  // the weight is streamed once
+    const uint64_t pol_x = l2_policy_evict_last();   // x is re-read by every row tile
+    const int npre = nkb < stages ? nkb : stages;
+    // The weight is never written by another kernel: fill the ring with it
+    // before waiting for the previous kernel in the stream.
+    for (int i = 0; i < npre; ++i) {
+      mbar_arrive_expect_tx(full0 + 8 * i, kStageWBytes + kStageXBytes);
+      tma_load_2d(smem_u32(s_w + i * kStageWBytes), &tmap_w, full0 + 8 * i, (kb0 + i) * kBlockK,
+                  n0, pol_w);
+    }
+    griddep_wait();
+    for (int i = 0; i < npre; ++i)
+      tma_load_2d(smem_u32(s_x + i * kStageXBytes), &tmap_x, full0 + 8 * i, (kb0 + i) * kBlockK,
+                  0, pol_x);
+    issued = npre;
+    for (int i = npre; i < nkb; ++i) {
+      const int s = i % stages;
+      const uint32_t par = ((i / stages) & 1) ^ 1;
+      if (!wait_or_abort(empty0 + 8 * s, par, abort_flag)) {
+        atomicOr(&g_device_status, SK_DEVICE_WAIT_PRODUCER);
+        *abort_flag = 1;
+        break;
+      }
+      mbar_arrive_expect_tx(full0 + 8 * s, kStageWBytes + kStageXBytes);
+      tma_load_2d(smem_u32(s_w + s * kStageWBytes), &tmap_w, full0 + 8 * s, (kb0 + i) * kBlockK,
+                  n0, pol_w);
+      tma_load_2d(smem_u32(s_x + s * kStageXBytes), &tmap_x, full0 + 8 * s, (kb0 + i) * kBlockK,
+                  0, pol_x);
+      issued = i + 1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------- MMA issuer
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % stages;
+      const uint32_t par = (i / stages) & 1;
+      if (!wait_or_abort(full0 + 8 * s, par, abort_flag)) {
+        atomicOr(&g_device_status, SK_DEVICE_WAIT_MMA);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint64_t adesc = smem_desc_k128(smem_u32(s_w + s * kStageWBytes));
+      const uint64_t bdesc = smem_desc_k128(smem_u32(s_x + s * kStageXBytes));
+#pragma unroll
+      for (int kk = 0; kk < kBlockK / 16; ++kk) {
+        // K advances 16 elements = 32 bytes inside the 128-byte swizzle row.
+        tc_mma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (i | kk) != 0);
+      }
+      tc_commit(empty0 + 8 * s);  // frees the stage once these MMAs have read it
+    }
+    tc_commit(done_bar);  // accumulator complete (or, after an abort, quiescent)
+  }
+  __syncwarp();
+
+  // ------------------------------------------------------------ epilogue
+  if (!mbar_wait_bounded(done_bar, 0, kWaitLimitNs)) {
+    atomicOr(&g_device_status, SK_DEVICE_WAIT_EPILOGUE);
+    *abort_flag = 1;
+  }
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // Do not leave copies in flight into shared memory this CTA releases.
+    const int first = issued > stages ? issued - stages : 0;
+    for (int j = first; j < issued; ++j)
+      mbar_wait_bounded(full0 + 8 * (j % stages), (j / stages) & 1, kWaitLimitNs);
+  }
+  __syncthreads();
+  const bool aborted = *abort_flag != 0;
+  tc_fence_after_sync();
+
+  float acc[kTokTile];
+  tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16), acc);
+
+  // Outputs may still be read by the previous kernel in the stream.
+  griddep_wait();
+
+  const int m = args.m, n = args.n;
+  uint16_t *y = args.y;
+  if (args.splits == 1) {
+    const int row = n0 + tid;
+    if (!aborted && row < n) {
+#pragma unroll
+      for (int t = 0; t < kTokTile; ++t)
+        if (t < m) y[static_cast<size_t>(t) * n + row] = bf16_store_bits(acc[t]);
+    }
+  } else {
+    // Split-K: each rank leaves its FP32 partial [token][row] in its own shared
+    // memory (the first ring stage, idle now), then rank r sums rows
+    // [r * R, (r + 1) * R) over ranks 0, 1, ..., S-1 in that order.
+    float *red = reinterpret_cast<float *>(s_w);
+    if (!aborted) {
+#pragma unroll
+      for (int t = 0; t < kTokTile; ++t)
+        if (t < m) red[t * kTileN + tid] = acc[t];
+    }
+    cluster_sync();
+    const int S = args.splits;
+    const int R = kTileN / S;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t red_base = smem_u32(red);
+    for (int o = tid; o < R * m; o += kGemmThreads) {
+      const int t = o / R;
+      const int row = static_cast<int>(rank) * R + o % R;
+      const uint32_t off = static_cast<uint32_t>((t * kTileN + row) * 4);
+      float v = dsmem_ld_f32(dsmem_map(red_base + off, 0));
+      for (int q = 1; q < S; ++q) v += dsmem_ld_f32(dsmem_map(red_base + off, q));
+      if (!aborted && n0 + row < n) y[static_cast<size_t>(t) * n + n0 + row] = bf16_store_bits(v);
+    }
+    cluster_sync();  // keep this CTA's shared memory alive until every rank has read it
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 2) tmem_dealloc(tmem, 32);
+}
+
+// ----------------------------------------------------------------------------
+// Block-wide FP32 sum in a fixed order: shuffle-down tree inside each warp,
+// then warp totals added in warp order by thread 0. `red` holds >= 33 floats.
+__device__ __forceinline__ float block_sum(float v, float *red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_down_sync(0xffffffffu, v, off);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = red[0];
+    const int nw = (blockDim.x + 31) >> 5;
+    for (int i = 1; i < nw; ++i) s += red[i];
+    red[32] = s;
+  }
+  __syncthreads();
+  return red[32];
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &v, uint16_t (&o)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[2 * i] = static_cast<uint16_t>(w[i] & 0xFFFFu);
+    o[2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const uint16_t (&o)[8]) {
+  uint4 v;
+  v.x = o[0] | (static_cast<uint32_t>(o[1]) << 16);
+  v.y = o[2] | (static_cast<uint32_t>(o[3]) << 16);
+  v.z = o[4] | (static_cast<uint32_t>(o[5]) << 16);
+  v.w = o[6] | (static_cast<uint32_t>(o[7]) << 16);
+  return v;
+}
+
+// NVFP4 of one 16-element block of BF16 values (cutedsl/moe/pooler_gather:
+// module docstring and nvfp4_compute_output_scale; the block-scale formula is
+// our reading, (amax / 6) * gs, since the pages print only its inverse).
+// Writes the 8 packed code bytes (column 2c in the low nibble) and returns the
+// e4m3 scale byte. Every step is an IEEE FP32 operation.
+__device__ __forceinline__ uint32_t nvfp4_block16(const uint16_t (&z)[16], float gs,
+                                                  uint2 &packed) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(bf16_bits_to_f32(z[j])));
+  const float t = __fmul_rn(__fdiv_rn(amax, 6.0f), gs);
+  const uint32_t sf = cvt_f32_e4m3(t);
+  const float sff = cvt_e4m3_f32(sf);
+  const float os = (sff == 0.0f) ? 0.0f : __fdiv_rn(1.0f, __fmul_rn(sff, __fdiv_rn(1.0f, gs)));
+  uint32_t b[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    b[c] = cvt_f32x2_e2m1x2(__fmul_rn(bf16_bits_to_f32(z[2 * c]), os),
+                            __fmul_rn(bf16_bits_to_f32(z[2 * c + 1]), os));
+  packed.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+  packed.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+  return sf;
+}
+
+// Pre-expert RMSNorm + NVFP4: one CTA per token row, one thread per 16-column
+// block (cutedsl/moe/pooler_gather, module docstring; pooler_layer: weight
+// applied after the norm).
+__global__ void __launch_bounds__(1024)
+    rmsnorm_nvfp4_kernel(const uint16_t *__restrict__ y, const uint16_t *__restrict__ norm_w,
+                         float eps, float gc, const float *__restrict__ gs_ptr,
+                         uint8_t *__restrict__ a, uint8_t *__restrict__ a_sf,
+                         uint16_t *__restrict__ z_out, int n) {
+  __shared__ float red[33];
+  const int row = blockIdx.x, blk = threadIdx.x;
+  const int nblk = n >> 4;
+  const bool active = blk < nblk;
+  griddep_launch_dependents();
+
+  uint16_t w[16];
+  if (active) {  // the norm weight is never written by a kernel: read it before the wait
+    const uint4 *wp = reinterpret_cast<const uint4 *>(norm_w + 16 * blk);
+    uint16_t lo[8], hi[8];
+    unpack8(__ldg(wp), lo);
+    unpack8(__ldg(wp + 1), hi);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      w[j] = lo[j];
+      w[8 + j] = hi[j];
+    }
+  }
+  griddep_wait();
+
+  uint16_t v[16];
+  float ss = 0.0f;
+  if (active) {
+    const uint4 *yp = reinterpret_cast<const uint4 *>(y + static_cast<size_t>(row) * n + 16 * blk);
+    uint16_t lo[8], hi[8];
+    unpack8(yp[0], lo);
+    unpack8(yp[1], hi);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] = lo[j];
+      v[8 + j] = hi[j];
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float f = bf16_bits_to_f32(v[j]);
+      ss = __fmaf_rn(f, f, ss);
+    }
+  }
+  ss = block_sum(ss, red);
+  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(n)), eps)));
+  if (!active) return;
+
+  uint16_t z[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float g = __fadd_rn(bf16_bits_to_f32(w[j]), gc);
+    z[j] = bf16_store_bits(__fmul_rn(__fmul_rn(bf16_bits_to_f32(v[j]), r), g));
+  }
+  const float gs = *gs_ptr;
+  uint2 packed;
+  const uint32_t sf = nvfp4_block16(z, gs, packed);
+  const size_t base = static_cast<size_t>(row) * n + 16 * blk;
+  reinterpret_cast<uint2 *>(a)[base >> 4] = packed;
+  a_sf[base >> 4] = static_cast<uint8_t>(sf);
+  if (z_out) {
+    uint16_t lo[8], hi[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      lo[j] = z[j];
+      hi[j] = z[8 + j];
+    }
+    uint4 *zp = reinterpret_cast<uint4 *>(z_out + base);
+    zp[0] = pack8(lo);
+    zp[1] = pack8(hi);
+  }
+}
+
+// NVFP4 of a BF16 [m, n] tensor: one thread per 16-element block.
+__global__ void __launch_bounds__(256)
+    nvfp4_quantize_kernel(const uint16_t *__restrict__ z, const float *__restrict__ gs_ptr,
+                          uint8_t *__restrict__ a, uint8_t *__restrict__ a_sf, int n) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int row = blockIdx.y;
+  const int blk = blockIdx.x * blockDim.x + threadIdx.x;
+  if (blk >= (n >> 4)) return;
+  const size_t base = static_cast<size_t>(row) * n + 16 * blk;
+  const uint4 *zp = reinterpret_cast<const uint4 *>(z + base);
+  uint16_t lo[8], hi[8], v[16];
+  unpack8(zp[0], lo);
+  unpack8(zp[1], hi);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    v[j] = lo[j];
+    v[8 + j] = hi[j];
+  }
+  uint2 packed;
+  const uint32_t sf = nvfp4_block16(v, *gs_ptr, packed);
+  reinterpret_cast<uint2 *>(a)[base >> 4] = packed;
+  a_sf[base >> 4] = static_cast<uint8_t>(sf);
+}
+
+// Attention-boundary dual norm (cutedsl/oproj/batt, AttentionBoundary): one CTA
+// per token row, one thread per 8 consecutive columns (h <= 8 * kDualThreads).
+constexpr int kDualThreads = 1024;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__global__ void __launch_bounds__(kDualThreads)
+    dual_norm_kernel(const uint16_t *__restrict__ p, float *__restrict__ s,
+                     const uint16_t *__restrict__ w1, float alpha,
+                     const uint16_t *__restrict__ beta, const uint16_t *__restrict__ w2,
+                     uint16_t *__restrict__ out, float eps_post, float eps_pre, float gc_post,
+                     float gc_pre, int h) {
+  __shared__ float red1[33], red2[33];
+  const int row = blockIdx.x, ch = threadIdx.x;
+  const bool active = ch < (h >> 3);
+  griddep_launch_dependents();
+
+  // Weights first (never written by a kernel), then wait for the producer of
+  // the partial and of the residual stream.
+  uint4 g1 = make_uint4(0, 0, 0, 0), gb = g1, g2 = g1;
+  if (active) {
+    if (w1) g1 = __ldg(reinterpret_cast<const uint4 *>(w1) + ch);
+    gb = __ldg(reinterpret_cast<const uint4 *>(beta) + ch);
+    g2 = __ldg(reinterpret_cast<const uint4 *>(w2) + ch);
+  }
+  griddep_wait();
+
+  const size_t rbase = static_cast<size_t>(row) * h;
+  float pv[8], sv[8];
+  float ss1 = 0.0f;
+  if (active) {
+    const uint4 pw = reinterpret_cast<const uint4 *>(p + rbase)[ch];
+    const float4 *sp = reinterpret_cast<const float4 *>(s + rbase) + 2 * ch;
+    const float4 s0 = sp[0], s1 = sp[1];
+    pv[0] = bf16_lo(pw.x); pv[1] = bf16_hi(pw.x); pv[2] = bf16_lo(pw.y); pv[3] = bf16_hi(pw.y);
+    pv[4] = bf16_lo(pw.z); pv[5] = bf16_hi(pw.z); pv[6] = bf16_lo(pw.w); pv[7] = bf16_hi(pw.w);
+    sv[0] = s0.x; sv[1] = s0.y; sv[2] = s0.z; sv[3] = s0.w;
+    sv[4] = s1.x; sv[5] = s1.y; sv[6] = s1.z; sv[7] = s1.w;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss1 = __fmaf_rn(pv[j], pv[j], ss1);
+  }
+  ss1 = block_sum(ss1, red1);
+  const float r1 =
+      __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss1, static_cast<float>(h)), eps_post)));
+
+  float ss2 = 0.0f;
+  if (active) {
+    const uint32_t w1w[4] = {g1.x, g1.y, g1.z, g1.w};
+    const uint32_t bw[4] = {gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t ww = w1w[j >> 1], bb = bw[j >> 1];
+      const float g = w1 ? __fadd_rn((j & 1) ? bf16_hi(ww) : bf16_lo(ww), gc_post) : 1.0f;
+      const float q = __fmul_rn(__fmul_rn(pv[j], r1), g);
+      const float bj = (j & 1) ? bf16_hi(bb) : bf16_lo(bb);
+      sv[j] = __fmaf_rn(bj, q, __fmul_rn(alpha, sv[j]));
+      ss2 = __fmaf_rn(sv[j], sv[j], ss2);
+    }
+    float4 *sp = reinterpret_cast<float4 *>(s + rbase) + 2 * ch;
+    sp[0] = make_float4(sv[0], sv[1], sv[2], sv[3]);
+    sp[1] = make_float4(sv[4], sv[5], sv[6], sv[7]);
+  }
+  ss2 = block_sum(ss2, red2);
+  const float r2 =
+      __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss2, static_cast<float>(h)), eps_pre)));
+
+  if (active) {
+    const uint32_t w2w[4] = {g2.x, g2.y, g2.z, g2.w};
+    uint16_t o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t ww = w2w[j >> 1];
+      const float g = __fadd_rn((j & 1) ? bf16_hi(ww) : bf16_lo(ww), gc_pre);
+      o[j] = bf16_store_bits(__fmul_rn(__fmul_rn(sv[j], r2), g));
+    }
+    reinterpret_cast<uint4 *>(out + rbase)[ch] = pack8(o);
+  }
+}
+
+// Format-conversion probe over n inputs (see sk_convert_probe).
+__global__ void convert_probe_kernel(int kind, const void *__restrict__ in, void *__restrict__ out,
+                                     int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    if (kind == 3) {
+      static_cast<float *>(out)[i] = cvt_e4m3_f32(static_cast<const uint8_t *>(in)[i]);
+      continue;
+    }
+    const float v = static_cast<const float *>(in)[i];
+    if (kind == 0) {
+      static_cast<uint8_t *>(out)[i] = static_cast<uint8_t>(cvt_f32x2_e2m1x2(v, 0.0f) & 0xFu);
+    } else if (kind == 1) {
+      static_cast<uint8_t *>(out)[i] = static_cast<uint8_t>(cvt_f32_e4m3(v));
+    } else {
+      static_cast<uint16_t *>(out)[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+size_t gemm_smem_bytes(int stages) {
+  return 1024 + static_cast<size_t>(stages) * (kStageWBytes + kStageXBytes) +
+         static_cast<size_t>(2 * stages + 1) * 8 + 16;
+}
+
+namespace {
+std::mutex g_setup_mutex;
+DeviceInfo g_info[64];
+bool g_ready[64];
+
+template <typename... Args>
+cudaError_t launch_ex(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t stream, bool pdl, int cluster_y,
+                      typename std::remove_reference<Args>::type... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  if (pdl) {
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (cluster_y > 1) {
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = 1;
+    attrs[na].val.clusterDim.y = static_cast<unsigned>(cluster_y);
+    attrs[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+}  // namespace
+
+cudaError_t device_setup(int device, DeviceInfo *info) {
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (!g_ready[device]) {
+    DeviceInfo d;
+    cudaError_t e;
+    int v = 0;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device))) return e;
+    d.sm_count = v;
+    if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, device))) return e;
+    if ((e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, device))) return e;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, device))) return e;
+    d.max_smem_optin = static_cast<size_t>(v);
+    if (d.major == 10 && d.minor == 3) {
+      const size_t want = gemm_smem_bytes(kMaxStages);
+      if ((e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(want))))
+        return e;
+      if ((e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)))
+        return e;
+    }
+    g_info[device] = d;
+    g_ready[device] = true;
+  }
+  *info = g_info[device];
+  return cudaSuccess;
+}
+
+cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, uint16_t *y, int m,
+                        int n, int k, int splits, int stages, cudaStream_t stream, bool pdl) {
+  GemmArgs a;
+  a.y = y;
+  a.m = m;
+  a.n = n;
+  a.kb_per_split = k / (kBlockK * splits);
+  a.stages = stages;
+  a.splits = splits;
+  const dim3 grid((n + kTileN - 1) / kTileN, splits, 1);
+  return launch_ex(gemm_kernel, grid, dim3(kGemmThreads), gemm_smem_bytes(stages), stream, pdl,
+                   splits, tmap_w, tmap_x, a);
+}
+
+cudaError_t launch_rmsnorm_nvfp4(const uint16_t *y, const uint16_t *norm_w, float eps, float gc,
+                                 const float *gs, uint8_t *a, uint8_t *a_sf, uint16_t *z_out,
+                                 int m, int n, cudaStream_t stream, bool pdl) {
+  const int threads = ((n / 16) + 31) / 32 * 32;
+  return launch_ex(rmsnorm_nvfp4_kernel, dim3(m), dim3(threads), 0, stream, pdl, 1, y, norm_w,
+                   eps, gc, gs, a, a_sf, z_out, n);
+}
+
+cudaError_t launch_nvfp4_quantize(const uint16_t *z, const float *gs, uint8_t *a, uint8_t *a_sf,
+                                  int m, int n, cudaStream_t stream, bool pdl) {
+  const int nblk = n / 16;
+  const dim3 grid((nblk + 255) / 256, m);
+  return launch_ex(nvfp4_quantize_kernel, grid, dim3(256), 0, stream, pdl, 1, z, gs, a, a_sf, n);
+}
+
+cudaError_t launch_dual_norm(const uint16_t *p, float *s, const uint16_t *w1, float alpha,
+                             const uint16_t *beta, const uint16_t *w2, uint16_t *out,
+                             float eps_post, float eps_pre, float gc_post, float gc_pre, int m,
+                             int h, cudaStream_t stream, bool pdl) {
+  const int threads = (h / 8 + 31) / 32 * 32;  // h <= 8 * kDualThreads (checked by the caller)
+  return launch_ex(dual_norm_kernel, dim3(m), dim3(threads), 0, stream, pdl, 1, p, s, w1, alpha,
+                   beta, w2, out, eps_post, eps_pre, gc_post, gc_pre, h);
+}
+
+cudaError_t launch_convert_probe(int kind, const void *in, void *out, int n, cudaStream_t stream) {
+  int blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  convert_probe_kernel<<<blocks, 256, 0, stream>>>(kind, in, out, n);
+  return cudaGetLastError();
+}
+
+cudaError_t read_device_status(uint32_t *out, bool clear) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e) return e;
+  if ((e = cudaMemcpyFromSymbol(out, g_device_status, sizeof(uint32_t)))) return e;
+  if (clear) {
+    const uint32_t zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(uint32_t)))) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace sk

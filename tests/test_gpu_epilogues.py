@@ -1,0 +1,215 @@
+"""GPU parity of the epilogues against the CPU oracle: the pre-expert RMSNorm +
+NVFP4 (standalone, fused behind the pooler GEMM, and the quantizer alone on
+the oracle's own z), and the attention-boundary dual norm (standalone and
+fused behind the o_proj GEMM). Every call goes through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from nvfp4_sm_skinny_gb300 import synth
+from parity import bf16_to_f64, check_gemm, check_nvfp4_end_to_end, ulp_distance
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def sk():
+    import nvfp4_sm_skinny_gb300 as sk
+
+    sk.lib()
+    return sk
+
+
+@pytest.fixture(autouse=True)
+def _no_device_errors(sk):
+    yield
+    assert sk.device_status(clear=True) == 0
+
+
+def gs_tensor(v):
+    return torch.tensor([v], dtype=torch.float32, device=DEV)
+
+
+def calibrated_gs(w, norm_w):
+    """Global scale from a seeded calibration batch through the oracle pipeline:
+    gs = 448 * 6 / amax(z_cal)."""
+    x_cal = synth.normal_bf16((16, w.shape[1]), 1.0, 1000)
+    y = oracle.gemm_bf16(synth.bits(x_cal), synth.bits(w))
+    z = oracle.rmsnorm_bf16(y, synth.bits(norm_w), synth.EPS, synth.GAIN_CENTER)
+    amax = float(np.max(np.abs(bf16_to_f64(z))))
+    return float(np.float32(2688.0 / amax))
+
+
+# ----------------------------------------------------------- NVFP4 alone ----
+@pytest.mark.parametrize("m,n,gs", [(1, 16, 1.0), (3, 4096, 500.0), (16, 4096, 2688.0 / 5),
+                                    (7, 1024, 1e4), (2, 160, 1e-3)])
+def test_quantize_bit_exact_on_oracle_z(sk, m, n, gs):
+    g = torch.Generator().manual_seed(m * n)
+    z = (torch.randn(m, n, generator=g) * torch.exp(torch.randn(m, 1, generator=g))).to(torch.bfloat16)
+    z[0, :16] = 0.0                                     # an all-zero block
+    if n >= 64:
+        z[-1, 32:48] = -z[-1, 32:48].abs() * 1e-4        # tiny negatives
+    zb = synth.bits(z)
+    zb = np.where(zb == 0x8000, 0, zb)
+    a_ref, sf_ref = oracle.nvfp4_quantize(zb, gs)
+    a, a_sf = sk.nvfp4_quantize(synth.from_bits(zb, DEV), gs_tensor(gs))
+    torch.cuda.synchronize()
+    assert np.array_equal(a_sf.cpu().numpy(), sf_ref)
+    assert np.array_equal(a.cpu().numpy(), a_ref)
+    assert np.all(sf_ref[0, 0] == 0) and np.all(a_ref[0, :8] == 0)
+
+
+# ---------------------------------------------------- RMSNorm + NVFP4 ----
+@pytest.mark.parametrize("m,n", [(1, 4096), (8, 4096), (16, 4096), (4, 48), (16, 16384)])
+def test_rmsnorm_nvfp4_standalone(sk, m, n):
+    y = synth.normal_bf16((m, n), 1.8, 40 + m)
+    w = synth.normal_bf16((n,), 0.1, 41)
+    gs = 2688.0 / 7.0
+    a, a_sf, z = sk.rmsnorm_nvfp4(y.to(DEV), w.to(DEV), synth.EPS, synth.GAIN_CENTER, gs_tensor(gs),
+                                  z_out=True)
+    torch.cuda.synchronize()
+    z_ref = oracle.rmsnorm_bf16(synth.bits(y), synth.bits(w), synth.EPS, synth.GAIN_CENTER)
+    d = ulp_distance(synth.bits(z), z_ref)
+    assert d.max() <= 1 and (d != 0).mean() < 1e-3
+    # NVFP4 decisions: bit-exact given the GPU's own z
+    a_ref, sf_ref = oracle.nvfp4_quantize(synth.bits(z), gs)
+    assert np.array_equal(a.cpu().numpy(), a_ref) and np.array_equal(a_sf.cpu().numpy(), sf_ref)
+    # end to end against the oracle's own z
+    a_ref2, sf_ref2 = oracle.nvfp4_quantize(z_ref, gs)
+    check_nvfp4_end_to_end(a.cpu().numpy(), a_sf.cpu().numpy(), synth.bits(z), a_ref2, sf_ref2, z_ref)
+
+
+def test_rmsnorm_zero_row_gives_zero_scale_and_codes(sk):
+    y = torch.zeros(2, 4096, dtype=torch.bfloat16, device=DEV)
+    w = synth.normal_bf16((4096,), 0.1, 41).to(DEV)
+    a, a_sf, z = sk.rmsnorm_nvfp4(y, w, synth.EPS, 1.0, gs_tensor(300.0), z_out=True)
+    torch.cuda.synchronize()
+    assert torch.all(a == 0) and torch.all(a_sf == 0) and torch.all(z.view(torch.int16) == 0)
+
+
+@pytest.mark.parametrize("b", [1, 8, 16])
+def test_pooler_gemm_rmsnorm_nvfp4(sk, b):
+    d = synth.pooler(b)
+    gs = calibrated_gs(d["w"], d["norm_w"])
+    a, a_sf, z, ws = sk.gemm_rmsnorm_nvfp4(d["x"].to(DEV), d["w"].to(DEV), d["norm_w"].to(DEV),
+                                           d["eps"], d["gain_center"], gs_tensor(gs), z_out=True)
+    torch.cuda.synchronize()
+    y_gpu = ws[: b * 4096 * 2].view(torch.bfloat16).view(b, 4096)
+    yb = synth.bits(y_gpu)
+    # 1. the GEMM
+    xb, wb = synth.bits(d["x"]), synth.bits(d["w"])
+    acc, absacc = oracle.gemm_f64(xb, wb)
+    y_ref = oracle.gemm_bf16(xb, wb)
+    check_gemm(yb, y_ref, acc, absacc, 8192, sk.gemm_splits(b, 4096, 8192))
+    # 2. the norm of the GPU's own y
+    z_tf = oracle.rmsnorm_bf16(yb, synth.bits(d["norm_w"]), d["eps"], d["gain_center"])
+    zd = ulp_distance(synth.bits(z), z_tf)
+    assert zd.max() <= 1
+    # 3. NVFP4 of the GPU's own z: bit-exact
+    a_tf, sf_tf = oracle.nvfp4_quantize(synth.bits(z), gs)
+    assert np.array_equal(a.cpu().numpy(), a_tf) and np.array_equal(a_sf.cpu().numpy(), sf_tf)
+    # 4. end to end from x
+    a_ref, sf_ref, z_ref, _ = oracle.gemm_rmsnorm_nvfp4(xb, wb, synth.bits(d["norm_w"]), d["eps"],
+                                                        d["gain_center"], gs)
+    check_nvfp4_end_to_end(a.cpu().numpy(), a_sf.cpu().numpy(), synth.bits(z), a_ref, sf_ref, z_ref)
+
+
+def test_pooler_saturates_beyond_calibration(sk):
+    d = synth.pooler(4)
+    gs = calibrated_gs(d["w"], d["norm_w"]) * 8      # scale too large: many blocks saturate
+    a, a_sf, z, _ = sk.gemm_rmsnorm_nvfp4(d["x"].to(DEV), d["w"].to(DEV), d["norm_w"].to(DEV),
+                                          d["eps"], d["gain_center"], gs_tensor(gs), z_out=True)
+    torch.cuda.synchronize()
+    a_tf, sf_tf = oracle.nvfp4_quantize(synth.bits(z), gs)
+    assert np.array_equal(a.cpu().numpy(), a_tf) and np.array_equal(a_sf.cpu().numpy(), sf_tf)
+    assert (sf_tf == 0x7E).any()
+
+
+# --------------------------------------------------------------- dual norm ----
+def _check_dual(sk, d, p_bits, s0, s_gpu, out_gpu, post_w):
+    s_ref, out_ref = oracle.dual_norm(p_bits, s0, None if post_w is None else synth.bits(post_w),
+                                      d["alpha"], synth.bits(d["beta"]), synth.bits(d["pre_w"]),
+                                      d["eps"], d["eps"])
+    # FP32 residual: 1e-5 relative to the summands alpha*s and beta*q
+    q_mag = np.abs(s_ref.astype(np.float64) - d["alpha"] * s0.astype(np.float64))
+    tol = 1e-5 * (np.abs(d["alpha"] * s0.astype(np.float64)) + q_mag + 1e-30)
+    err = np.abs(s_gpu.astype(np.float64) - s_ref.astype(np.float64))
+    assert np.all(err <= tol), float(np.max(err / tol))
+    # output: the pre-FFN norm of the GPU's own stream, within one BF16 ulp
+    zero_beta = np.zeros(s0.shape[1], np.uint16)
+    _, out_tf = oracle.dual_norm(np.zeros_like(p_bits), s_gpu, None, 1.0, zero_beta,
+                                 synth.bits(d["pre_w"]), d["eps"], d["eps"])
+    assert ulp_distance(synth.bits(out_gpu), out_tf).max() <= 1
+    # and end to end against the oracle (cancellation in s makes a few
+    # outputs differ by more than an ulp only where s ~ 0)
+    dd = ulp_distance(synth.bits(out_gpu), out_ref)
+    assert (dd > 1).mean() < 1e-3
+
+
+@pytest.mark.parametrize("b", [1, 4, 16])
+@pytest.mark.parametrize("with_post", [True, False])
+def test_dual_norm_standalone(sk, b, with_post):
+    d = synth.oproj_boundary(b)
+    p = synth.normal_bf16((b, 8192), 1.5, 60 + b)
+    post_w = d["post_w"] if with_post else None
+    s_dev = d["stream"].to(DEV)
+    out = sk.dual_norm_residual(p.to(DEV), s_dev, None if post_w is None else post_w.to(DEV),
+                                d["alpha"], d["beta"].to(DEV), d["pre_w"].to(DEV),
+                                eps_post=d["eps"], eps_pre=d["eps"])
+    torch.cuda.synchronize()
+    _check_dual(sk, d, synth.bits(p), d["stream"].numpy(), s_dev.cpu().numpy(), out, post_w)
+
+
+def test_dual_norm_small_width_and_alpha(sk):
+    g = torch.Generator().manual_seed(9)
+    h = 72
+    p = torch.randn(3, h, generator=g).to(torch.bfloat16)
+    s = torch.randn(3, h, generator=g)
+    beta = torch.rand(h, generator=g).to(torch.bfloat16)
+    w1 = (1 + 0.1 * torch.randn(h, generator=g)).to(torch.bfloat16)
+    w2 = (1 + 0.1 * torch.randn(h, generator=g)).to(torch.bfloat16)
+    s_dev = s.to(DEV)
+    out = sk.dual_norm_residual(p.to(DEV), s_dev, w1.to(DEV), 0.5, beta.to(DEV), w2.to(DEV),
+                                eps_post=1e-5, eps_pre=1e-6, gc_post=0.25, gc_pre=0.5)
+    torch.cuda.synchronize()
+    s_ref, out_ref = oracle.dual_norm(synth.bits(p), s.numpy(), synth.bits(w1), 0.5, synth.bits(beta),
+                                      synth.bits(w2), 1e-5, 1e-6, 0.25, 0.5)
+    assert np.allclose(s_dev.cpu().numpy(), s_ref, rtol=1e-5, atol=1e-6)
+    assert ulp_distance(synth.bits(out), out_ref).max() <= 1
+
+
+@pytest.mark.parametrize("b", [1, 4, 16])
+def test_oproj_gemm_dual_norm(sk, b):
+    d = synth.oproj_boundary(b)
+    s_dev = d["stream"].to(DEV)
+    out, ws = sk.gemm_dual_norm(d["x"].to(DEV), d["w"].to(DEV), s_dev, d["post_w"].to(DEV),
+                                d["alpha"], d["beta"].to(DEV), d["pre_w"].to(DEV),
+                                eps_post=d["eps"], eps_pre=d["eps"])
+    torch.cuda.synchronize()
+    p_gpu = synth.bits(ws[: b * 8192 * 2].view(torch.bfloat16).view(b, 8192))
+    xb, wb = synth.bits(d["x"]), synth.bits(d["w"])
+    acc, absacc = oracle.gemm_f64(xb, wb)
+    check_gemm(p_gpu, oracle.gemm_bf16(xb, wb), acc, absacc, 1024, sk.gemm_splits(b, 8192, 1024))
+    _check_dual(sk, d, p_gpu, d["stream"].numpy(), s_dev.cpu().numpy(), out, d["post_w"])
+
+
+def test_epilogues_bitwise_reproducible(sk):
+    d = synth.pooler(16)
+    x, w, nw = d["x"].to(DEV), d["w"].to(DEV), d["norm_w"].to(DEV)
+    gs = gs_tensor(300.0)
+    a0, s0, z0, _ = sk.gemm_rmsnorm_nvfp4(x, w, nw, d["eps"], 1.0, gs, z_out=True)
+    for _ in range(20):
+        a, s, z, _ = sk.gemm_rmsnorm_nvfp4(x, w, nw, d["eps"], 1.0, gs, z_out=True)
+        assert torch.equal(a, a0) and torch.equal(s, s0) and torch.equal(z.view(torch.int16), z0.view(torch.int16))
+    e = synth.oproj_boundary(16)
+    base = e["stream"].to(DEV)
+    outs = []
+    for _ in range(20):
+        s_dev = base.clone()
+        out, _ = sk.gemm_dual_norm(e["x"].to(DEV), e["w"].to(DEV), s_dev, e["post_w"].to(DEV), 1.0,
+                                   e["beta"].to(DEV), e["pre_w"].to(DEV))
+        outs.append((out.view(torch.int16).clone(), s_dev.clone()))
+    for o, s in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(s, outs[0][1])
