@@ -179,6 +179,35 @@ sk_status sk_gemm_dual_norm(const void *x, const void *w, float *resid, const vo
                             void *workspace, size_t workspace_bytes, int m, int n, int k,
                             int splits, void *stream);
 
+/* Bytes of the static device scratch behind sk_gemm_rmsnorm_nvfp4_static:
+   room for a BF16 [m, n] GEMM output with m * n <= 131072 (16 x 8192). */
+#define SK_STATIC_SCRATCH_BYTES (16u * 8192u * 2u)
+
+/*
+ * sk_gemm_rmsnorm_nvfp4_static -- sk_gemm_rmsnorm_nvfp4 without a workspace
+ * argument, for callers that cannot allocate device memory: an inference-
+ * engine plugin whose enqueue function is handed no workspace, code that is
+ * being recorded into a CUDA graph (cudaMalloc cannot be captured), or a
+ * serving loop whose memory is budgeted once at start-up. The pages have no
+ * counterpart to this call; it is an addition of this library.
+ *   Same arguments, results and constraints as sk_gemm_rmsnorm_nvfp4, less
+ *   workspace/workspace_bytes, plus m * n <= SK_STATIC_SCRATCH_BYTES / 2:
+ *   larger shapes are rejected with SK_ERR_INVALID_ARG before any launch.
+ *   The GEMM output goes to a fixed array in the library's device image (one
+ *   per device that loads the library, held until the process exits). The
+ *   call allocates nothing.
+ *   The first call on a device looks up that array's device address (once per
+ *   device, with the device current); make that first call before any stream
+ *   capture. Every call shares the array and it keeps the last call's
+ *   contents; it needs no clearing, since the GEMM rewrites what the norm then
+ *   reads. Calls that may run at the same time on the GPU (unordered streams)
+ *   race on the array and give wrong results.
+ */
+sk_status sk_gemm_rmsnorm_nvfp4_static(const void *x, const void *w, const void *norm_w,
+                                       float eps, float gain_center, const float *global_scale,
+                                       uint8_t *a, uint8_t *a_sf, void *z_out, int m, int n,
+                                       int k, int splits, void *stream);
+
 /*
  * sk_device_status -- HOST-synchronizing diagnostic: copies the library's
  * device status word (an OR of SK_DEVICE_WAIT_* bits set by kernels whose

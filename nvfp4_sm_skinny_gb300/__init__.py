@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
             "sk_dual_norm_residual": ([vp, vp, vp, f, vp, vp, vp, f, f, f, f, i, i, vp], i),
             "sk_gemm_dual_norm_workspace": ([i, i], sz),
             "sk_gemm_dual_norm": ([vp, vp, vp, vp, f, vp, vp, vp, f, f, f, f, vp, sz, i, i, i, i, vp], i),
+            "sk_gemm_rmsnorm_nvfp4_static": ([vp, vp, vp, f, f, vp, vp, vp, vp, i, i, i, i, vp], i),
             "sk_device_status": ([ctypes.POINTER(ctypes.c_uint32), i], i),
             "sk_convert_probe": ([i, vp, vp, i, vp], i),
         }
@@ -203,6 +204,30 @@ def gemm_rmsnorm_nvfp4(x, w, norm_w, eps: float, gain_center: float, global_scal
         _ptr(z_out), _ptr(workspace), workspace.numel() * workspace.element_size(), m, n, k,
         splits, _stream(stream)))
     return a, a_sf, z_out, workspace
+
+
+STATIC_SCRATCH_BYTES = 16 * 8192 * 2
+
+
+def gemm_rmsnorm_nvfp4_static(x, w, norm_w, eps: float, gain_center: float, global_scale, a,
+                              a_sf, z_out=None, splits: int = 0, stream=None):
+    """The pooler call without a workspace (the library's static device
+    scratch holds the GEMM output; m * n <= 131072). The caller passes every
+    output; nothing is allocated."""
+    m, k = x.shape
+    n = w.shape[0]
+    _need(x, torch.bfloat16, (m, k), "x")
+    _need(w, torch.bfloat16, (n, k), "w")
+    _need(norm_w, torch.bfloat16, (n,), "norm_w")
+    _need(global_scale, torch.float32, (1,), "global_scale")
+    _need(a, torch.uint8, (m, n // 2), "a")
+    _need(a_sf, torch.uint8, (m, n // 16), "a_sf")
+    if z_out is not None:
+        _need(z_out, torch.bfloat16, (m, n), "z_out")
+    _check(lib().sk_gemm_rmsnorm_nvfp4_static(
+        _ptr(x), _ptr(w), _ptr(norm_w), eps, gain_center, _ptr(global_scale), _ptr(a), _ptr(a_sf),
+        _ptr(z_out), m, n, k, splits, _stream(stream)))
+    return a, a_sf, z_out
 
 
 def nvfp4_quantize(z, global_scale, a=None, a_sf=None, stream=None):

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsk.so")
 
-SOURCES = ["sk_api.cu", "sk_kernels.cu"]
+SOURCES = ["sk_api.cu", "sk_kernels.cu", "sk_static_scratch.cu"]
 HEADERS = ["sk_internal.h", "sk_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -170,6 +170,8 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
 }  // namespace
 
+sk_status sk::report_error(sk_status st, const char *msg) { return fail(st, "%s", msg); }
+
 extern "C" {
 
 const char *sk_last_error(void) { return t_last_error.c_str(); }

@@ -7,7 +7,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "sk.h"
+
 namespace sk {
+
+// Records `msg` as this thread's sk_last_error() and returns `st`.
+sk_status report_error(sk_status st, const char *msg);
 
 // GEMM tiling: each CTA owns kTileN consecutive weight rows (output features)
 // and one K slice; the tensor-core instruction is M = kTileN weight rows by
