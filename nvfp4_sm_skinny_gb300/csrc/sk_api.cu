@@ -108,29 +108,65 @@ sk_status check_gemm_shape(int m, int n, int k, int splits) {
   return SK_OK;
 }
 
-// Automatic split count: the largest S in {1, 2, 4, 8, 16} that divides K into
-// whole 64-wide blocks while tiles x S stays within one CTA per SM. A single
-// row tile (small n) may use up to 16 ranks.
-int auto_splits(int n, int k, int sm_count) {
-  const int tiles = (n + sk::kTileN - 1) / sk::kTileN;
-  int best = 1;
-  for (int s = 2; s <= 16; s *= 2) {
-    if (k % (sk::kBlockK * s)) break;
-    if (tiles * s > sm_count) break;
-    best = s;
-  }
-  return best;
+// Launch plan of the GEMM for one shape.
+struct GemmPlan {
+  int splits;  // K slices (cluster ranks)
+  int h;       // weight rows per CTA
+  int stages;  // pipeline stages per CTA
+};
+
+int env_int(const char *name, int lo, int hi) {
+  const char *v = std::getenv(name);
+  if (!v || !v[0]) return 0;
+  const int x = std::atoi(v);
+  return (x >= lo && x <= hi) ? x : 0;
 }
 
-int choose_stages(int n, int k, int splits, int sm_count) {
-  const int nkb = k / (sk::kBlockK * splits);
-  const int tiles = (n + sk::kTileN - 1) / sk::kTileN;
-  int st = tiles * splits <= sm_count ? sk::kMaxStages : 5;  // 5 stages: two CTAs fit an SM
-  if (const char *v = std::getenv("SK_STAGES")) {
-    const int forced = std::atoi(v);
-    if (forced >= 1 && forced <= sk::kMaxStages) st = forced;
+// The weight stream is the whole cost; what sets its rate is the number of
+// bytes in flight from HBM (tens of MB GPU-wide) and the size of each copy.
+// Long K (>= 2048): full 128-row tiles, and the largest split count S that
+// keeps every CTA resident at two per SM (tiles x S <= 2 x SMs, clusters
+// schedulable) with at least 8 K blocks per CTA; short K: no split, one wave
+// of CTAs one per SM with the rows spread evenly. The ring takes all the
+// shared memory the residency allows. A requested split count is honoured.
+GemmPlan plan_gemm(int n, int k, int splits_req, int device, int sm_count) {
+  GemmPlan p{0, 0, 0};
+  const int nkb_total = k / sk::kBlockK;
+  auto fits = [&](int s, int tiles, int per_sm) {
+    if (tiles * s > per_sm * sm_count) return false;
+    if (s == 1) return true;
+    const int c = sk::gemm_max_clusters(device, s, per_sm);
+    return c <= 0 || tiles <= c;
+  };
+  if (splits_req) {
+    p.splits = splits_req;
+    const int cap = 2 * sm_count / splits_req;
+    int h = (n + (cap > 0 ? cap : 1) - 1) / (cap > 0 ? cap : 1);
+    p.h = h < 16 ? 16 : (h > sk::kMmaM ? sk::kMmaM : h);
+    if (k >= 2048) p.h = sk::kMmaM;
+  } else if (k >= 2048) {
+    p.h = sk::kMmaM;
+    const int tiles = (n + p.h - 1) / p.h;
+    p.splits = 1;
+    for (int s = 2; s <= 16; s *= 2) {
+      if (nkb_total % s || nkb_total / s < 8) break;
+      if (!fits(s, tiles, 2)) break;
+      p.splits = s;
+    }
+  } else {
+    p.splits = 1;
+    int h = (n + sm_count - 1) / sm_count;
+    p.h = h < 16 ? 16 : (h > sk::kMmaM ? sk::kMmaM : h);
   }
-  return st < nkb ? st : nkb;
+  if (const int hv = env_int("SK_TILE_ROWS", 16, sk::kMmaM)) p.h = hv;
+  const int tiles = (n + p.h - 1) / p.h;
+  const size_t budget = tiles * p.splits <= sm_count ? sk::kOnePerSmSmem : sk::kTwoPerSmSmem;
+  int st = 1;
+  while (st < sk::kMaxStages && sk::gemm_smem_bytes(p.h, st + 1) <= budget) ++st;
+  if (const int sv = env_int("SK_STAGES", 1, sk::kMaxStages)) st = sv;
+  const int nst = (nkb_total / p.splits + sk::kBoxesPerStage - 1) / sk::kBoxesPerStage;
+  p.stages = st < nst ? st : nst;
+  return p;
 }
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -143,14 +179,17 @@ sk_status launch_status(cudaError_t e, const char *what) {
 // Validated GEMM enqueue shared by the three GEMM entry points.
 sk_status enqueue_gemm(const void *x, const void *w, void *y, int m, int n, int k, int splits,
                        void *stream, const sk::DeviceInfo &info) {
-  const int s = splits ? splits : auto_splits(n, k, info.sm_count);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const GemmPlan plan = plan_gemm(n, k, splits, dev, info.sm_count);
+  if (plan.splits == 0)
+    return fail(SK_ERR_UNSUPPORTED, "no GEMM launch for n=%d, k=%d, splits=%d", n, k, splits);
   CUtensorMap tw, tx;
   sk_status st;
-  if ((st = make_map(&tw, w, n, k, sk::kTileN)) != SK_OK) return st;
+  if ((st = make_map(&tw, w, n, k, plan.h)) != SK_OK) return st;
   if ((st = make_map(&tx, x, m, k, sk::kTokTile)) != SK_OK) return st;
-  const int stages = choose_stages(n, k, s, info.sm_count);
-  return launch_status(sk::launch_gemm(tw, tx, static_cast<uint16_t *>(y), m, n, k, s, stages,
-                                       as_stream(stream), pdl_enabled()),
+  return launch_status(sk::launch_gemm(tw, tx, static_cast<uint16_t *>(y), m, n, k, plan.splits,
+                                       plan.h, plan.stages, as_stream(stream), pdl_enabled()),
                        "gemm");
 }
 
@@ -188,8 +227,10 @@ int sk_gemm_splits(int m, int n, int k, int splits) {
   if (splits) return splits;
   sk::DeviceInfo info;
   if (current_device(&info) != SK_OK) return 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
   ok();
-  return auto_splits(n, k, info.sm_count);
+  return plan_gemm(n, k, 0, dev, info.sm_count).splits;
 }
 
 sk_status sk_gemm_bf16(const void *x, const void *w, void *y, int m, int n, int k, int splits,

@@ -14,16 +14,50 @@ namespace sk {
 // Records `msg` as this thread's sk_last_error() and returns `st`.
 sk_status report_error(sk_status st, const char *msg);
 
-// GEMM tiling: each CTA owns kTileN consecutive weight rows (output features)
-// and one K slice; the tensor-core instruction is M = kTileN weight rows by
-// N = kTokTile token columns (rows of x beyond m are zero-filled by the copy
-// engine), K = 16 per instruction, kBlockK per pipeline stage.
-constexpr int kTileN = 128;
+// GEMM tiling. Each CTA owns h <= kMmaM consecutive weight rows (output
+// features) and one K slice. The tensor-core instruction is M = kMmaM weight
+// rows by N = kTokTile token columns by K = 16 (rows of x beyond m are
+// zero-filled by the copy engine; tile rows beyond h hold stale data whose
+// accumulator lanes are never stored). Each pipeline stage moves
+// kBoxesPerStage boxes of kBlockK columns: a weight box of h rows (its slot is
+// h rounded up to 8 rows, 1 KiB per 8 rows) and an activation box of 16 rows.
+constexpr int kMmaM = 128;
 constexpr int kTokTile = 16;
 constexpr int kBlockK = 64;
-constexpr int kStageWBytes = kTileN * kBlockK * 2;   // 16 KiB weight box
-constexpr int kStageXBytes = kTokTile * kBlockK * 2; // 2 KiB activation box
-constexpr int kMaxStages = 12;
+constexpr int kBoxesPerStage = 2;
+constexpr int kSlotXBytes = kTokTile * kBlockK * 2;  // 2 KiB
+constexpr int kMmaABytes = kMmaM * kBlockK * 2;      // 16 KiB read by one MMA row block
+constexpr int kMaxStages = 16;
+// Shared memory per CTA when two CTAs share an SM.
+constexpr size_t kTwoPerSmSmem = 110 * 1024;
+// Shared memory per CTA when one CTA owns an SM.
+constexpr size_t kOnePerSmSmem = 220 * 1024;
+
+// Shared-memory layout of a GEMM CTA, relative to its 1024-aligned base:
+// weight slots [0, w_end), activation slots [x_off, x_end), barriers at
+// bar_off. The data region also covers the 16 KiB an MMA reads from the last
+// weight slot and the 8 KiB split-K partial parked in the ring after the loop.
+struct GemmLayout {
+  int slot_w;  // bytes per weight slot
+  int x_off;   // first activation slot
+  int bar_off; // mbarriers (2 * stages + 1), then the TMEM address and a flag
+  int total;   // bytes from the aligned base to the end of the flag words
+};
+
+__host__ __device__ inline GemmLayout gemm_layout(int h, int stages) {
+  GemmLayout L;
+  L.slot_w = ((h + 7) / 8) * 1024;
+  const int nslot = stages * kBoxesPerStage;
+  L.x_off = nslot * L.slot_w;
+  int end = L.x_off + nslot * kSlotXBytes;
+  const int mma_end = (nslot - 1) * L.slot_w + kMmaABytes;
+  const int red_end = kTokTile * kMmaM * 4;
+  if (mma_end > end) end = mma_end;
+  if (red_end > end) end = red_end;
+  L.bar_off = (end + 7) / 8 * 8;
+  L.total = L.bar_off + (2 * stages + 1) * 8 + 8;
+  return L;
+}
 
 struct DeviceInfo {
   int sm_count = 0;
@@ -35,12 +69,17 @@ struct DeviceInfo {
 // device. Returns cudaSuccess or the first error.
 cudaError_t device_setup(int device, DeviceInfo *info);
 
-size_t gemm_smem_bytes(int stages);
+// Dynamic shared memory of a GEMM CTA with tile height h and `stages` stages.
+size_t gemm_smem_bytes(int h, int stages);
 
-// Launches the split-K GEMM: grid (ceil(n / kTileN), splits), cluster
-// (1, splits, 1); `stages` pipeline stages per CTA.
+// Largest number of clusters of `splits` GEMM CTAs that can be resident at
+// once with `ctas_per_sm` (1 or 2) GEMM CTAs per SM (cached).
+int gemm_max_clusters(int device, int splits, int ctas_per_sm);
+
+// Launches the split-K GEMM: grid (ceil(n / h), splits), cluster
+// (1, splits, 1); tile height h rows, `stages` pipeline stages per CTA.
 cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, uint16_t *y, int m,
-                        int n, int k, int splits, int stages, cudaStream_t stream, bool pdl);
+                        int n, int k, int splits, int h, int stages, cudaStream_t stream, bool pdl);
 
 cudaError_t launch_rmsnorm_nvfp4(const uint16_t *y, const uint16_t *norm_w, float eps, float gc,
                                  const float *gs, uint8_t *a, uint8_t *a_sf, uint16_t *z_out,

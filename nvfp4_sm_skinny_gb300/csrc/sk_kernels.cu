@@ -21,13 +21,14 @@ namespace sk {
 // OR of SK_DEVICE_WAIT_* bits, set by kernels whose bounded waits ran out.
 __device__ uint32_t g_device_status;
 
-constexpr uint32_t kIdesc = idesc_bf16_f32(kTileN, kTokTile);
+constexpr uint32_t kIdesc = idesc_bf16_f32(kMmaM, kTokTile);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s of wall time per wait
 constexpr int kGemmThreads = 128;                  // 4 warps = the 128 TMEM lanes
 
 struct GemmArgs {
-  uint16_t *y;   // [m, n] BF16 bits
+  uint16_t *y;       // [m, n] BF16 bits
   int m, n;
+  int h;             // weight rows per CTA (tile height), 1..kMmaM
   int kb_per_split;  // kBlockK-wide K blocks per CTA
   int stages;
   int splits;
@@ -45,7 +46,8 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
   return true;
 }
 
-// One CTA = kTileN weight rows x one K slice of kb_per_split * 64 elements.
+// One CTA = h weight rows x one K slice of kb_per_split * 64 elements, moved
+// kBoxesPerStage 64-column boxes per pipeline stage.
 // Warp 0 lane 0: TMA producer. Warp 1 lane 0: MMA issuer. Warp 2 owns the
 // TMEM allocation. All four warps run the epilogue (one TMEM lane per thread).
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -54,17 +56,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  constexpr int B = kBoxesPerStage;
   const int stages = args.stages;
-  uint8_t *s_w = smem;                                   // stages x 16 KiB (1024-aligned)
-  uint8_t *s_x = smem + stages * kStageWBytes;           // stages x 2 KiB (1024-aligned)
-  uint64_t *bars = reinterpret_cast<uint64_t *>(s_x + stages * kStageXBytes);
+  const GemmLayout lay = gemm_layout(args.h, stages);
+  const int slot_w = lay.slot_w;
+  uint8_t *s_w = smem;                                     // stages*B weight slots
+  uint8_t *s_x = smem + lay.x_off;                         // stages*B activation slots
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * stages + 1);
   volatile uint32_t *abort_flag = tmem_slot + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * kTileN;
+  const int h = args.h;
+  const int n0 = blockIdx.x * h;
   const int nkb = args.kb_per_split;
   const int kb0 = blockIdx.y * nkb;
+  const int nst = (nkb + B - 1) / B;                     // pipeline stages of work
+  const uint32_t box_tx = static_cast<uint32_t>(h * 128 + kSlotXBytes);
 
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = smem_u32(bars + stages);
@@ -99,20 +107,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---------------------------------------------------- TMA producer
     const uint64_t pol_w = l2_policy_evict_first();  // the weight is streamed once
     const uint64_t pol_x = l2_policy_evict_last();   // x is re-read by every row tile
-    const int npre = nkb < stages ? nkb : stages;
+    const int npre = nst < stages ? nst : stages;
     // The weight is never written by another kernel: fill the ring with it
     // before waiting for the previous kernel in the stream.
     for (int i = 0; i < npre; ++i) {
-      mbar_arrive_expect_tx(full0 + 8 * i, kStageWBytes + kStageXBytes);
-      tma_load_2d(smem_u32(s_w + i * kStageWBytes), &tmap_w, full0 + 8 * i, (kb0 + i) * kBlockK,
-                  n0, pol_w);
+      const int nb = min(B, nkb - i * B);
+      mbar_arrive_expect_tx(full0 + 8 * i, nb * box_tx);
+      for (int j = 0; j < nb; ++j)
+        tma_load_2d(smem_u32(s_w + (i * B + j) * slot_w), &tmap_w, full0 + 8 * i,
+                    (kb0 + i * B + j) * kBlockK, n0, pol_w);
     }
     griddep_wait();
-    for (int i = 0; i < npre; ++i)
-      tma_load_2d(smem_u32(s_x + i * kStageXBytes), &tmap_x, full0 + 8 * i, (kb0 + i) * kBlockK,
-                  0, pol_x);
+    for (int i = 0; i < npre; ++i) {
+      const int nb = min(B, nkb - i * B);
+      for (int j = 0; j < nb; ++j)
+        tma_load_2d(smem_u32(s_x + (i * B + j) * kSlotXBytes), &tmap_x, full0 + 8 * i,
+                    (kb0 + i * B + j) * kBlockK, 0, pol_x);
+    }
     issued = npre;
-    for (int i = npre; i < nkb; ++i) {
+    for (int i = npre; i < nst; ++i) {
       const int s = i % stages;
       const uint32_t par = ((i / stages) & 1) ^ 1;
       if (!wait_or_abort(empty0 + 8 * s, par, abort_flag)) {
@@ -120,16 +133,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         *abort_flag = 1;
         break;
       }
-      mbar_arrive_expect_tx(full0 + 8 * s, kStageWBytes + kStageXBytes);
-      tma_load_2d(smem_u32(s_w + s * kStageWBytes), &tmap_w, full0 + 8 * s, (kb0 + i) * kBlockK,
-                  n0, pol_w);
-      tma_load_2d(smem_u32(s_x + s * kStageXBytes), &tmap_x, full0 + 8 * s, (kb0 + i) * kBlockK,
-                  0, pol_x);
+      const int nb = min(B, nkb - i * B);
+      mbar_arrive_expect_tx(full0 + 8 * s, nb * box_tx);
+      for (int j = 0; j < nb; ++j) {
+        const int kc = (kb0 + i * B + j) * kBlockK;
+        tma_load_2d(smem_u32(s_w + (s * B + j) * slot_w), &tmap_w, full0 + 8 * s, kc, n0, pol_w);
+        tma_load_2d(smem_u32(s_x + (s * B + j) * kSlotXBytes), &tmap_x, full0 + 8 * s, kc, 0, pol_x);
+      }
       issued = i + 1;
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------- MMA issuer
-    for (int i = 0; i < nkb; ++i) {
+    for (int i = 0; i < nst; ++i) {
       const int s = i % stages;
       const uint32_t par = (i / stages) & 1;
       if (!wait_or_abort(full0 + 8 * s, par, abort_flag)) {
@@ -138,12 +153,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const uint64_t adesc = smem_desc_k128(smem_u32(s_w + s * kStageWBytes));
-      const uint64_t bdesc = smem_desc_k128(smem_u32(s_x + s * kStageXBytes));
+      const int nb = min(B, nkb - i * B);
+      for (int j = 0; j < nb; ++j) {
+        const uint64_t adesc = smem_desc_k128(smem_u32(s_w + (s * B + j) * slot_w));
+        const uint64_t bdesc = smem_desc_k128(smem_u32(s_x + (s * B + j) * kSlotXBytes));
 #pragma unroll
-      for (int kk = 0; kk < kBlockK / 16; ++kk) {
-        // K advances 16 elements = 32 bytes inside the 128-byte swizzle row.
-        tc_mma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (i | kk) != 0);
+        for (int kk = 0; kk < kBlockK / 16; ++kk) {
+          // K advances 16 elements = 32 bytes inside the 128-byte swizzle row.
+          tc_mma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (i | j | kk) != 0);
+        }
       }
       tc_commit(empty0 + 8 * s);  // frees the stage once these MMAs have read it
     }
@@ -176,30 +194,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint16_t *y = args.y;
   if (args.splits == 1) {
     const int row = n0 + tid;
-    if (!aborted && row < n) {
+    if (!aborted && tid < h && row < n) {
 #pragma unroll
       for (int t = 0; t < kTokTile; ++t)
         if (t < m) y[static_cast<size_t>(t) * n + row] = bf16_store_bits(acc[t]);
     }
   } else {
     // Split-K: each rank leaves its FP32 partial [token][row] in its own shared
-    // memory (the first ring stage, idle now), then rank r sums rows
+    // memory (the first ring slot, idle now), then rank r sums tile rows
     // [r * R, (r + 1) * R) over ranks 0, 1, ..., S-1 in that order.
     float *red = reinterpret_cast<float *>(s_w);
     if (!aborted) {
 #pragma unroll
       for (int t = 0; t < kTokTile; ++t)
-        if (t < m) red[t * kTileN + tid] = acc[t];
+        if (t < m) red[t * kMmaM + tid] = acc[t];
     }
     cluster_sync();
     const int S = args.splits;
-    const int R = kTileN / S;
+    const int R = (h + S - 1) / S;
     const uint32_t rank = cluster_ctarank();
     const uint32_t red_base = smem_u32(red);
     for (int o = tid; o < R * m; o += kGemmThreads) {
       const int t = o / R;
       const int row = static_cast<int>(rank) * R + o % R;
-      const uint32_t off = static_cast<uint32_t>((t * kTileN + row) * 4);
+      if (row >= h) continue;
+      const uint32_t off = static_cast<uint32_t>((t * kMmaM + row) * 4);
       float v = dsmem_ld_f32(dsmem_map(red_base + off, 0));
       for (int q = 1; q < S; ++q) v += dsmem_ld_f32(dsmem_map(red_base + off, q));
       if (!aborted && n0 + row < n) y[static_cast<size_t>(t) * n + n0 + row] = bf16_store_bits(v);
@@ -473,9 +492,8 @@ __global__ void convert_probe_kernel(int kind, const void *__restrict__ in, void
 }
 
 // ---------------------------------------------------------------- host side
-size_t gemm_smem_bytes(int stages) {
-  return 1024 + static_cast<size_t>(stages) * (kStageWBytes + kStageXBytes) +
-         static_cast<size_t>(2 * stages + 1) * 8 + 16;
+size_t gemm_smem_bytes(int h, int stages) {
+  return 1024 + static_cast<size_t>(gemm_layout(h, stages).total);
 }
 
 namespace {
@@ -526,7 +544,7 @@ cudaError_t device_setup(int device, DeviceInfo *info) {
     if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, device))) return e;
     d.max_smem_optin = static_cast<size_t>(v);
     if (d.major == 10 && d.minor == 3) {
-      const size_t want = gemm_smem_bytes(kMaxStages);
+      const size_t want = d.max_smem_optin;
       if ((e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(want))))
         return e;
@@ -540,17 +558,48 @@ cudaError_t device_setup(int device, DeviceInfo *info) {
   return cudaSuccess;
 }
 
+int gemm_max_clusters(int device, int splits, int ctas_per_sm) {
+  static std::mutex mu;
+  static int cache[64][5][2];
+  int idx = 0;
+  while ((1 << idx) < splits && idx < 4) ++idx;
+  const int per = ctas_per_sm >= 2 ? 1 : 0;
+  if (device < 0 || device >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[device][idx][per] == 0) {
+    int clusters = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, splits, 1);
+    cfg.blockDim = dim3(kGemmThreads);
+    // more than half an SM's shared memory: one CTA per SM; else two
+    cfg.dynamicSmemBytes = per ? 100 * 1024 : 120 * 1024;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 1;
+    attr.val.clusterDim.y = static_cast<unsigned>(splits);
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_kernel, &cfg) != cudaSuccess || clusters < 1)
+      clusters = -1;
+    cache[device][idx][per] = clusters;
+  }
+  return cache[device][idx][per];
+}
+
 cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, uint16_t *y, int m,
-                        int n, int k, int splits, int stages, cudaStream_t stream, bool pdl) {
+                        int n, int k, int splits, int h, int stages, cudaStream_t stream,
+                        bool pdl) {
   GemmArgs a;
   a.y = y;
   a.m = m;
   a.n = n;
+  a.h = h;
   a.kb_per_split = k / (kBlockK * splits);
   a.stages = stages;
   a.splits = splits;
-  const dim3 grid((n + kTileN - 1) / kTileN, splits, 1);
-  return launch_ex(gemm_kernel, grid, dim3(kGemmThreads), gemm_smem_bytes(stages), stream, pdl,
+  const dim3 grid((n + h - 1) / h, splits, 1);
+  return launch_ex(gemm_kernel, grid, dim3(kGemmThreads), gemm_smem_bytes(h, stages), stream, pdl,
                    splits, tmap_w, tmap_x, a);
 }
 
