@@ -36,7 +36,8 @@ constexpr size_t kOnePerSmSmem = 220 * 1024;
 // Shared-memory layout of a GEMM CTA, relative to its 1024-aligned base:
 // weight slots [0, w_end), activation slots [x_off, x_end), barriers at
 // bar_off. The data region also covers the 16 KiB an MMA reads from the last
-// weight slot and the 8 KiB split-K partial parked in the ring after the loop.
+// weight slot and the split-K partials the ranks push into the ring after the
+// loop (16 tokens x (h + S) rows of FP32 at most).
 struct GemmLayout {
   int slot_w;  // bytes per weight slot
   int x_off;   // first activation slot
@@ -51,7 +52,7 @@ __host__ __device__ inline GemmLayout gemm_layout(int h, int stages) {
   L.x_off = nslot * L.slot_w;
   int end = L.x_off + nslot * kSlotXBytes;
   const int mma_end = (nslot - 1) * L.slot_w + kMmaABytes;
-  const int red_end = kTokTile * kMmaM * 4;
+  const int red_end = kTokTile * (kMmaM + 16) * 4;  // split-K partials, all ranks
   if (mma_end > end) end = mma_end;
   if (red_end > end) end = red_end;
   L.bar_off = (end + 7) / 8 * 8;

@@ -9,6 +9,7 @@
 // cutedsl/moe/pooler_gather (module docstring: pre-expert norm and NVFP4
 // layout; nvfp4_compute_output_scale and the cvt helpers), and
 // cutedsl/oproj/batt (AttentionBoundary: the dual norm).
+#include <cstdlib>
 #include <mutex>
 #include <type_traits>
 
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncwarp();
 
   // ------------------------------------------------------------ epilogue
-  if (!mbar_wait_bounded(done_bar, 0, kWaitLimitNs)) {
+  if (!mbar_wait_idle(done_bar, 0, kWaitLimitNs)) {
     atomicOr(&g_device_status, SK_DEVICE_WAIT_EPILOGUE);
     *abort_flag = 1;
   }
@@ -200,30 +201,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (t < m) y[static_cast<size_t>(t) * n + row] = bf16_store_bits(acc[t]);
     }
   } else {
-    // Split-K: each rank leaves its FP32 partial [token][row] in its own shared
-    // memory (the first ring slot, idle now), then rank r sums tile rows
-    // [r * R, (r + 1) * R) over ranks 0, 1, ..., S-1 in that order.
-    float *red = reinterpret_cast<float *>(s_w);
-    if (!aborted) {
-#pragma unroll
-      for (int t = 0; t < kTokTile; ++t)
-        if (t < m) red[t * kMmaM + tid] = acc[t];
-    }
-    cluster_sync();
+    // Split-K across the S ranks of the cluster. Rank r owns tile rows
+    // [r * R, (r + 1) * R). Once every rank's MMAs are done (its ring is idle),
+    // each rank pushes its FP32 partial of every row into the owner's ring:
+    // red[q][t][row - r * R] for source rank q and token t. The owner then sums
+    // q = 0, 1, ..., S-1 in that order from its own shared memory.
     const int S = args.splits;
     const int R = (h + S - 1) / S;
     const uint32_t rank = cluster_ctarank();
+    float *red = reinterpret_cast<float *>(s_w);
     const uint32_t red_base = smem_u32(red);
+    cluster_sync();  // all ranks past their MMAs
+    if (!aborted && tid < h) {
+      const uint32_t owner = static_cast<uint32_t>(tid / R);
+      const int lr = tid - static_cast<int>(owner) * R;
+      const uint32_t dst = dsmem_map(red_base + static_cast<uint32_t>((rank * kTokTile * R + lr) * 4),
+                                     owner);
+#pragma unroll
+      for (int t = 0; t < kTokTile; ++t)
+        if (t < m) dsmem_st_f32(dst + static_cast<uint32_t>(t * R * 4), acc[t]);
+    }
+    cluster_sync();  // partials visible to their owners; no remote access after this
     for (int o = tid; o < R * m; o += kGemmThreads) {
       const int t = o / R;
-      const int row = static_cast<int>(rank) * R + o % R;
+      const int lr = o - t * R;
+      const int row = static_cast<int>(rank) * R + lr;
       if (row >= h) continue;
-      const uint32_t off = static_cast<uint32_t>((t * kMmaM + row) * 4);
-      float v = dsmem_ld_f32(dsmem_map(red_base + off, 0));
-      for (int q = 1; q < S; ++q) v += dsmem_ld_f32(dsmem_map(red_base + off, q));
+      float v = red[t * R + lr];
+      for (int q = 1; q < S; ++q) v += red[(q * kTokTile + t) * R + lr];
       if (!aborted && n0 + row < n) y[static_cast<size_t>(t) * n + n0 + row] = bf16_store_bits(v);
     }
-    cluster_sync();  // keep this CTA's shared memory alive until every rank has read it
   }
 
   tc_fence_before_sync();
@@ -248,6 +255,20 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
   }
   __syncthreads();
   return red[32];
+}
+
+// Sum over the CTAs of a (csize, 1, 1) cluster of one value per CTA, in rank
+// order, so every CTA gets the same bits. `slot` is this CTA's shared word;
+// other ranks read it after the barrier, so the caller keeps the CTA alive
+// (a later cluster barrier) until they are done.
+__device__ __forceinline__ float cluster_total(float cta_part, float *slot, unsigned csize) {
+  if (csize == 1) return cta_part;
+  if (threadIdx.x == 0) *slot = cta_part;
+  cluster_sync();
+  const uint32_t a = smem_u32(slot);
+  float t = dsmem_ld_f32(dsmem_map(a, 0));
+  for (unsigned q = 1; q < csize; ++q) t += dsmem_ld_f32(dsmem_map(a, q));
+  return t;
 }
 
 __device__ __forceinline__ void unpack8(const uint4 &v, uint16_t (&o)[8]) {
@@ -292,18 +313,21 @@ __device__ __forceinline__ uint32_t nvfp4_block16(const uint16_t (&z)[16], float
   return sf;
 }
 
-// Pre-expert RMSNorm + NVFP4: one CTA per token row, one thread per 16-column
-// block (cutedsl/moe/pooler_gather, module docstring; pooler_layer: weight
-// applied after the norm).
+// Pre-expert RMSNorm + NVFP4 (cutedsl/moe/pooler_gather, module docstring;
+// pooler_layer: weight applied after the norm). Token row i is spread over the
+// gridDim.x CTAs of one cluster; each thread owns one 16-column NVFP4 block.
 __global__ void __launch_bounds__(1024)
     rmsnorm_nvfp4_kernel(const uint16_t *__restrict__ y, const uint16_t *__restrict__ norm_w,
                          float eps, float gc, const float *__restrict__ gs_ptr,
                          uint8_t *__restrict__ a, uint8_t *__restrict__ a_sf,
                          uint16_t *__restrict__ z_out, int n) {
   __shared__ float red[33];
-  const int row = blockIdx.x, blk = threadIdx.x;
-  const int nblk = n >> 4;
-  const bool active = blk < nblk;
+  __shared__ float slot;
+  const unsigned csize = gridDim.x;
+  const int row = blockIdx.y;
+  const int per_cta = (n >> 4) / static_cast<int>(csize);
+  const int blk = blockIdx.x * per_cta + threadIdx.x;
+  const bool active = static_cast<int>(threadIdx.x) < per_cta;
   griddep_launch_dependents();
 
   uint16_t w[16];
@@ -338,33 +362,36 @@ __global__ void __launch_bounds__(1024)
       ss = __fmaf_rn(f, f, ss);
     }
   }
-  ss = block_sum(ss, red);
+  ss = cluster_total(block_sum(ss, red), &slot, csize);
+  if (csize > 1) cluster_arrive();  // done reading the other ranks' slots
   const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(n)), eps)));
-  if (!active) return;
 
-  uint16_t z[16];
+  if (active) {
+    uint16_t z[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float g = __fadd_rn(bf16_bits_to_f32(w[j]), gc);
-    z[j] = bf16_store_bits(__fmul_rn(__fmul_rn(bf16_bits_to_f32(v[j]), r), g));
-  }
-  const float gs = *gs_ptr;
-  uint2 packed;
-  const uint32_t sf = nvfp4_block16(z, gs, packed);
-  const size_t base = static_cast<size_t>(row) * n + 16 * blk;
-  reinterpret_cast<uint2 *>(a)[base >> 4] = packed;
-  a_sf[base >> 4] = static_cast<uint8_t>(sf);
-  if (z_out) {
-    uint16_t lo[8], hi[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      lo[j] = z[j];
-      hi[j] = z[8 + j];
+    for (int j = 0; j < 16; ++j) {
+      const float g = __fadd_rn(bf16_bits_to_f32(w[j]), gc);
+      z[j] = bf16_store_bits(__fmul_rn(__fmul_rn(bf16_bits_to_f32(v[j]), r), g));
     }
-    uint4 *zp = reinterpret_cast<uint4 *>(z_out + base);
-    zp[0] = pack8(lo);
-    zp[1] = pack8(hi);
+    const float gs = *gs_ptr;
+    uint2 packed;
+    const uint32_t sf = nvfp4_block16(z, gs, packed);
+    const size_t base = static_cast<size_t>(row) * n + 16 * blk;
+    reinterpret_cast<uint2 *>(a)[base >> 4] = packed;
+    a_sf[base >> 4] = static_cast<uint8_t>(sf);
+    if (z_out) {
+      uint16_t lo[8], hi[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        lo[j] = z[j];
+        hi[j] = z[8 + j];
+      }
+      uint4 *zp = reinterpret_cast<uint4 *>(z_out + base);
+      zp[0] = pack8(lo);
+      zp[1] = pack8(hi);
+    }
   }
+  if (csize > 1) cluster_wait();  // keep `slot` alive until every rank has read it
 }
 
 // NVFP4 of a BF16 [m, n] tensor: one thread per 16-element block.
@@ -392,8 +419,9 @@ __global__ void __launch_bounds__(256)
   a_sf[base >> 4] = static_cast<uint8_t>(sf);
 }
 
-// Attention-boundary dual norm (cutedsl/oproj/batt, AttentionBoundary): one CTA
-// per token row, one thread per 8 consecutive columns (h <= 8 * kDualThreads).
+// Attention-boundary dual norm (cutedsl/oproj/batt, AttentionBoundary). Token
+// row i is spread over the gridDim.x CTAs of one cluster; each thread owns 8
+// consecutive columns.
 constexpr int kDualThreads = 1024;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -406,8 +434,12 @@ __global__ void __launch_bounds__(kDualThreads)
                      uint16_t *__restrict__ out, float eps_post, float eps_pre, float gc_post,
                      float gc_pre, int h) {
   __shared__ float red1[33], red2[33];
-  const int row = blockIdx.x, ch = threadIdx.x;
-  const bool active = ch < (h >> 3);
+  __shared__ float slot1, slot2;
+  const unsigned csize = gridDim.x;
+  const int row = blockIdx.y;
+  const int per_cta = (h >> 3) / static_cast<int>(csize);
+  const int ch = blockIdx.x * per_cta + threadIdx.x;
+  const bool active = static_cast<int>(threadIdx.x) < per_cta;
   griddep_launch_dependents();
 
   // Weights first (never written by a kernel), then wait for the producer of
@@ -434,7 +466,7 @@ __global__ void __launch_bounds__(kDualThreads)
 #pragma unroll
     for (int j = 0; j < 8; ++j) ss1 = __fmaf_rn(pv[j], pv[j], ss1);
   }
-  ss1 = block_sum(ss1, red1);
+  ss1 = cluster_total(block_sum(ss1, red1), &slot1, csize);
   const float r1 =
       __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss1, static_cast<float>(h)), eps_post)));
 
@@ -455,7 +487,8 @@ __global__ void __launch_bounds__(kDualThreads)
     sp[0] = make_float4(sv[0], sv[1], sv[2], sv[3]);
     sp[1] = make_float4(sv[4], sv[5], sv[6], sv[7]);
   }
-  ss2 = block_sum(ss2, red2);
+  ss2 = cluster_total(block_sum(ss2, red2), &slot2, csize);
+  if (csize > 1) cluster_arrive();  // done reading the other ranks' slots
   const float r2 =
       __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss2, static_cast<float>(h)), eps_pre)));
 
@@ -470,6 +503,7 @@ __global__ void __launch_bounds__(kDualThreads)
     }
     reinterpret_cast<uint4 *>(out + rbase)[ch] = pack8(o);
   }
+  if (csize > 1) cluster_wait();  // keep the slots alive until every rank has read them
 }
 
 // Format-conversion probe over n inputs (see sk_convert_probe).
@@ -503,7 +537,7 @@ bool g_ready[64];
 
 template <typename... Args>
 cudaError_t launch_ex(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem,
-                      cudaStream_t stream, bool pdl, int cluster_y,
+                      cudaStream_t stream, bool pdl, dim3 cluster,
                       typename std::remove_reference<Args>::type... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -517,11 +551,11 @@ cudaError_t launch_ex(void (*kernel)(Args...), dim3 grid, dim3 block, size_t sme
     attrs[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
-  if (cluster_y > 1) {
+  if (cluster.x * cluster.y * cluster.z > 1) {
     attrs[na].id = cudaLaunchAttributeClusterDimension;
-    attrs[na].val.clusterDim.x = 1;
-    attrs[na].val.clusterDim.y = static_cast<unsigned>(cluster_y);
-    attrs[na].val.clusterDim.z = 1;
+    attrs[na].val.clusterDim.x = cluster.x;
+    attrs[na].val.clusterDim.y = cluster.y;
+    attrs[na].val.clusterDim.z = cluster.z;
     ++na;
   }
   cfg.attrs = attrs;
@@ -600,31 +634,53 @@ cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, ui
   a.splits = splits;
   const dim3 grid((n + h - 1) / h, splits, 1);
   return launch_ex(gemm_kernel, grid, dim3(kGemmThreads), gemm_smem_bytes(h, stages), stream, pdl,
-                   splits, tmap_w, tmap_x, a);
+                   dim3(1, splits, 1), tmap_w, tmap_x, a);
+}
+
+// CTAs per token row of the norm kernels (a cluster): 1 by default (measured
+// fastest: the kernels are latency-bound and a cluster barrier costs more than
+// it saves); SK_TAIL_CLUSTER (1, 2, 4 or 8) overrides.
+static int tail_cluster_max() {
+  static const int c = [] {
+    const char *v = std::getenv("SK_TAIL_CLUSTER");
+    const int x = v ? std::atoi(v) : 1;
+    return (x == 1 || x == 2 || x == 4 || x == 8) ? x : 1;
+  }();
+  return c;
 }
 
 cudaError_t launch_rmsnorm_nvfp4(const uint16_t *y, const uint16_t *norm_w, float eps, float gc,
                                  const float *gs, uint8_t *a, uint8_t *a_sf, uint16_t *z_out,
                                  int m, int n, cudaStream_t stream, bool pdl) {
-  const int threads = ((n / 16) + 31) / 32 * 32;
-  return launch_ex(rmsnorm_nvfp4_kernel, dim3(m), dim3(threads), 0, stream, pdl, 1, y, norm_w,
-                   eps, gc, gs, a, a_sf, z_out, n);
+  // a cluster of up to 8 CTAs per token row, at least one warp of blocks each
+  const int nblk = n / 16;
+  int c = tail_cluster_max();
+  while (c > 1 && (nblk % c || nblk / c < 32)) c /= 2;
+  const int threads = (nblk / c + 31) / 32 * 32;
+  return launch_ex(rmsnorm_nvfp4_kernel, dim3(c, m), dim3(threads), 0, stream, pdl, dim3(c, 1, 1),
+                   y, norm_w, eps, gc, gs, a, a_sf, z_out, n);
 }
 
 cudaError_t launch_nvfp4_quantize(const uint16_t *z, const float *gs, uint8_t *a, uint8_t *a_sf,
                                   int m, int n, cudaStream_t stream, bool pdl) {
   const int nblk = n / 16;
   const dim3 grid((nblk + 255) / 256, m);
-  return launch_ex(nvfp4_quantize_kernel, grid, dim3(256), 0, stream, pdl, 1, z, gs, a, a_sf, n);
+  return launch_ex(nvfp4_quantize_kernel, grid, dim3(256), 0, stream, pdl, dim3(1, 1, 1), z, gs, a,
+                   a_sf, n);
 }
 
 cudaError_t launch_dual_norm(const uint16_t *p, float *s, const uint16_t *w1, float alpha,
                              const uint16_t *beta, const uint16_t *w2, uint16_t *out,
                              float eps_post, float eps_pre, float gc_post, float gc_pre, int m,
                              int h, cudaStream_t stream, bool pdl) {
-  const int threads = (h / 8 + 31) / 32 * 32;  // h <= 8 * kDualThreads (checked by the caller)
-  return launch_ex(dual_norm_kernel, dim3(m), dim3(threads), 0, stream, pdl, 1, p, s, w1, alpha,
-                   beta, w2, out, eps_post, eps_pre, gc_post, gc_pre, h);
+  // a cluster of up to 8 CTAs per token row, at least two warps of chunks each
+  // (h <= 8 * kDualThreads is checked by the caller)
+  const int nchunk = h / 8;
+  int c = tail_cluster_max();
+  while (c > 1 && (nchunk % c || nchunk / c < 64)) c /= 2;
+  const int threads = (nchunk / c + 31) / 32 * 32;
+  return launch_ex(dual_norm_kernel, dim3(c, m), dim3(threads), 0, stream, pdl, dim3(c, 1, 1), p, s,
+                   w1, alpha, beta, w2, out, eps_post, eps_pre, gc_post, gc_pre, h);
 }
 
 cudaError_t launch_convert_probe(int kind, const void *in, void *out, int n, cudaStream_t stream) {
