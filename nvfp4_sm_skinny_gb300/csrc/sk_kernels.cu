@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_map(&tmap_x);
   }
   if (warp == 2) {
-    tmem_alloc(smem_u32(tmem_slot), 32);
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
@@ -160,8 +160,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint64_t bdesc = smem_desc_k128(smem_u32(s_x + (s * B + j) * kSlotXBytes));
 #pragma unroll
         for (int kk = 0; kk < kBlockK / 16; ++kk) {
-          // K advances 16 elements = 32 bytes inside the 128-byte swizzle row.
-          tc_mma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (i | j | kk) != 0);
+          // K advances 16 elements = 32 bytes inside the 128-byte swizzle row;
+          // each (box, k-step) of a stage has its own accumulator.
+          tc_mma_bf16(tmem + static_cast<uint32_t>((j * 4 + kk) * kTokTile), adesc + 2 * kk,
+                      bdesc + 2 * kk, kIdesc, i != 0);
         }
       }
       tc_commit(empty0 + 8 * s);  // frees the stage once these MMAs have read it
@@ -186,7 +188,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after_sync();
 
   float acc[kTokTile];
-  tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16), acc);
+  // accumulators of the second box are used only if the slice has two boxes
+  tmem_sum_accumulators<kNumAcc>(tmem + (static_cast<uint32_t>(warp * 32) << 16),
+                                 nkb >= 2 ? kNumAcc : kNumAcc / 2, acc);
 
   // Outputs may still be read by the previous kernel in the stream.
   griddep_wait();
@@ -235,7 +239,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 2) tmem_dealloc(tmem, 32);
+  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ----------------------------------------------------------------------------
@@ -525,6 +529,12 @@ __global__ void convert_probe_kernel(int kind, const void *__restrict__ in, void
   }
 }
 
+}  // namespace sk
+
+#include "sk_decode.cuh"
+
+namespace sk {
+
 // ---------------------------------------------------------------- host side
 size_t gemm_smem_bytes(int h, int stages) {
   return 1024 + static_cast<size_t>(gemm_layout(h, stages).total);
@@ -578,11 +588,17 @@ cudaError_t device_setup(int device, DeviceInfo *info) {
     if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, device))) return e;
     d.max_smem_optin = static_cast<size_t>(v);
     if (d.major == 10 && d.minor == 3) {
-      const size_t want = d.max_smem_optin;
+      // dynamic shared memory up to the opt-in limit less each kernel's static part
+      cudaFuncAttributes fa;
+      if ((e = cudaFuncGetAttributes(&fa, gemm_kernel))) return e;
       if ((e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(want))))
+                                    static_cast<int>(d.max_smem_optin - fa.sharedSizeBytes))))
         return e;
       if ((e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)))
+        return e;
+      if ((e = cudaFuncGetAttributes(&fa, decode_layer_kernel))) return e;
+      if ((e = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(d.max_smem_optin - fa.sharedSizeBytes))))
         return e;
     }
     g_info[device] = d;
@@ -702,4 +718,14 @@ cudaError_t read_device_status(uint32_t *out, bool clear) {
   return cudaSuccess;
 }
 
+}  // namespace sk
+
+namespace sk {
+int decode_blocks_per_sm(size_t smem) {
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, decode_layer_kernel, kDecThreads, smem) !=
+      cudaSuccess)
+    return 0;
+  return nb;
+}
 }  // namespace sk

@@ -190,6 +190,21 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, float (&v)[16
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Sum of the kNumAcc accumulators (16 columns each) of this thread's TMEM lane,
+// in accumulator order; accumulators >= n_used were never written.
+template <int NACC>
+__device__ __forceinline__ void tmem_sum_accumulators(uint32_t taddr, int n_used, float (&acc)[16]) {
+  tmem_ld_32x32b_x16(taddr, acc);
+#pragma unroll
+  for (int q = 1; q < NACC; ++q) {
+    if (q >= n_used) break;
+    float v[16];
+    tmem_ld_32x32b_x16(taddr + static_cast<uint32_t>(q * 16), v);
+#pragma unroll
+    for (int t = 0; t < 16; ++t) acc[t] = __fadd_rn(acc[t], v[t]);
+  }
+}
+
 // Shared-memory matrix descriptor for a K-major BF16 tile written by TMA with
 // 128-byte swizzling: rows of 64 elements (128 B), 8-row groups 1024 B apart.
 // Bits: [0,14) start >> 4, [16,30) leading offset >> 4 (unused for this
