@@ -6,6 +6,7 @@
 // string.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -113,6 +114,7 @@ struct GemmPlan {
   int splits;  // K slices (cluster ranks)
   int h;       // weight rows per CTA
   int stages;  // pipeline stages per CTA
+  int bps;     // 64-column boxes per stage
 };
 
 int env_int(const char *name, int lo, int hi) {
@@ -120,6 +122,29 @@ int env_int(const char *name, int lo, int hi) {
   if (!v || !v[0]) return 0;
   const int x = std::atoi(v);
   return (x >= lo && x <= hi) ? x : 0;
+}
+
+// Ring shape for a K slice of nkb boxes: the largest boxes-per-stage count that
+// still leaves three stages in flight (or holds the whole slice), then as many
+// stages as the shared-memory budget holds. SK_BPS / SK_STAGES override.
+template <typename Bytes>
+void choose_ring(int nkb, size_t budget, Bytes bytes, int *stages, int *bps) {
+  int best_b = 1;
+  for (int b = sk::kMaxBoxesPerStage; b >= 1; --b) {
+    if (b > nkb && b > 1) continue;
+    const int need = std::min(3, (nkb + b - 1) / b);
+    if (bytes(need, b) <= budget) {
+      best_b = b;
+      break;
+    }
+  }
+  if (const int bv = env_int("SK_BPS", 1, sk::kMaxBoxesPerStage)) best_b = bv;
+  int st = 1;
+  while (st < sk::kMaxStages && bytes(st + 1, best_b) <= budget) ++st;
+  if (const int sv = env_int("SK_STAGES", 1, sk::kMaxStages)) st = sv;
+  const int nst = (nkb + best_b - 1) / best_b;
+  *stages = st < nst ? st : nst;
+  *bps = best_b;
 }
 
 // The weight stream is the whole cost; what sets its rate is the number of
@@ -130,7 +155,7 @@ int env_int(const char *name, int lo, int hi) {
 // of CTAs one per SM with the rows spread evenly. The ring takes all the
 // shared memory the residency allows. A requested split count is honoured.
 GemmPlan plan_gemm(int n, int k, int splits_req, int device, int sm_count) {
-  GemmPlan p{0, 0, 0};
+  GemmPlan p{0, 0, 0, 1};
   const int nkb_total = k / sk::kBlockK;
   auto fits = [&](int s, int tiles, int per_sm) {
     if (tiles * s > per_sm * sm_count) return false;
@@ -161,11 +186,8 @@ GemmPlan plan_gemm(int n, int k, int splits_req, int device, int sm_count) {
   if (const int hv = env_int("SK_TILE_ROWS", 16, sk::kMmaM)) p.h = hv;
   const int tiles = (n + p.h - 1) / p.h;
   const size_t budget = tiles * p.splits <= sm_count ? sk::kOnePerSmSmem : sk::kTwoPerSmSmem;
-  int st = 1;
-  while (st < sk::kMaxStages && sk::gemm_smem_bytes(p.h, st + 1) <= budget) ++st;
-  if (const int sv = env_int("SK_STAGES", 1, sk::kMaxStages)) st = sv;
-  const int nst = (nkb_total / p.splits + sk::kBoxesPerStage - 1) / sk::kBoxesPerStage;
-  p.stages = st < nst ? st : nst;
+  choose_ring(nkb_total / p.splits, budget,
+              [&](int st, int b) { return sk::gemm_smem_bytes(p.h, st, b); }, &p.stages, &p.bps);
   return p;
 }
 
@@ -189,7 +211,8 @@ sk_status enqueue_gemm(const void *x, const void *w, void *y, int m, int n, int 
   if ((st = make_map(&tw, w, n, k, plan.h)) != SK_OK) return st;
   if ((st = make_map(&tx, x, m, k, sk::kTokTile)) != SK_OK) return st;
   return launch_status(sk::launch_gemm(tw, tx, static_cast<uint16_t *>(y), m, n, k, plan.splits,
-                                       plan.h, plan.stages, as_stream(stream), pdl_enabled()),
+                                       plan.h, plan.stages, plan.bps, as_stream(stream),
+                                       pdl_enabled()),
                        "gemm");
 }
 
@@ -451,10 +474,14 @@ sk_status sk_decode_layer(const void *h_in, const void *w_o, const void *w_p, co
   }
   args.slot_w = slot_w;
   const size_t cap = info.max_smem_optin - 1024;
-  int stages = 1;
-  while (stages < 32 && sk::decode_smem_bytes(slot_w, stages + 1) <= cap) ++stages;
-  args.stages = stages;
-  const size_t smem = sk::decode_smem_bytes(slot_w, stages);
+  const int nkb_max = std::max(args.nkb[0], std::max(args.nkb[1], args.nkb[2]));
+  choose_ring(nkb_max, cap, [&](int s, int b) { return sk::decode_smem_bytes(slot_w, s, b); },
+              &args.stages, &args.bps);
+  // the ring serves every phase in turn: keep all of its stages
+  while (args.stages < sk::kMaxStages &&
+         sk::decode_smem_bytes(slot_w, args.stages + 1, args.bps) <= cap)
+    ++args.stages;
+  const size_t smem = sk::decode_smem_bytes(slot_w, args.stages, args.bps);
   if (sk::decode_blocks_per_sm(smem) < 1)
     return fail(SK_ERR_UNSUPPORTED, "the fused layer kernel cannot be resident with %zu bytes", smem);
   args.post_w = static_cast<const uint16_t *>(post_w);

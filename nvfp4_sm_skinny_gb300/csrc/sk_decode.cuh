@@ -154,10 +154,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  constexpr int B = kBoxesPerStage;
+  const int B = args.bps;
   const int S = args.stages;
   const int slot_w = args.slot_w;
-  const DecodeLayout lay = decode_layout(slot_w, S);
+  const DecodeLayout lay = decode_layout(slot_w, S, B);
   uint8_t *s_w = smem;
   uint8_t *s_x = smem + lay.x_off;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
@@ -304,8 +304,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             const uint64_t bdesc = smem_desc_k128(smem_u32(s_x + (s * B + j) * kSlotXBytes));
 #pragma unroll
             for (int kk = 0; kk < kBlockK / 16; ++kk)
-              tc_mma_bf16(tmem + static_cast<uint32_t>((j * 4 + kk) * kTokTile), adesc + 2 * kk,
-                          bdesc + 2 * kk, kIdesc, ls != 0);
+              tc_mma_bf16(tmem + static_cast<uint32_t>(acc_index(j, kk) * kTokTile), adesc + 2 * kk,
+                          bdesc + 2 * kk, kIdesc, ls != 0 || j >= kNumAcc / 4);
           }
           tc_commit(empty0 + 8 * s);
         }
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         atomicExch(args.gabort, 1u);
       }
       tc_fence_after_sync();
-      tmem_sum_accumulators<kNumAcc>(taddr, args.nkb[0] >= 2 ? kNumAcc : kNumAcc / 2, v);
+      tmem_sum_accumulators<kNumAcc>(taddr, acc_used(args.nkb[0], B), v);
       tc_fence_before_sync();
 #pragma unroll
       for (int t = 0; t < 16; ++t) pv[t] = (valid0 && t < m) ? bf16_round_f32(v[t]) : 0.0f;
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         atomicExch(args.gabort, 1u);
       }
       tc_fence_after_sync();
-      tmem_sum_accumulators<kNumAcc>(taddr, args.nkb[1] >= 2 ? kNumAcc : kNumAcc / 2, v);
+      tmem_sum_accumulators<kNumAcc>(taddr, acc_used(args.nkb[1], B), v);
       tc_fence_before_sync();
 #pragma unroll
       for (int t = 0; t < 16; ++t) yv[t] = (valid1 && t < m) ? bf16_round_f32(v[t]) : 0.0f;
@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         atomicExch(args.gabort, 1u);
       }
       tc_fence_after_sync();
-      tmem_sum_accumulators<kNumAcc>(taddr, args.nkb[2] >= 2 ? kNumAcc : kNumAcc / 2, v);
+      tmem_sum_accumulators<kNumAcc>(taddr, acc_used(args.nkb[2], B), v);
       tc_fence_before_sync();
       if (e < h2 && n2 < H && !*abort_flag) {
 #pragma unroll
@@ -512,8 +512,8 @@ cudaError_t launch_decode_layer(const DecodeMaps &maps, const DecodeArgs &args, 
   return cudaLaunchKernelEx(&cfg, decode_layer_kernel, maps, args);
 }
 
-size_t decode_smem_bytes(int slot_w, int stages) {
-  return 1024 + static_cast<size_t>(decode_layout(slot_w, stages).total);
+size_t decode_smem_bytes(int slot_w, int stages, int bps) {
+  return 1024 + static_cast<size_t>(decode_layout(slot_w, stages, bps).total);
 }
 
 }  // namespace sk

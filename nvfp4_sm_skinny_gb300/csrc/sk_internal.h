@@ -18,22 +18,32 @@ sk_status report_error(sk_status st, const char *msg);
 // features) and one K slice. The tensor-core instruction is M = kMmaM weight
 // rows by N = kTokTile token columns by K = 16 (rows of x beyond m are
 // zero-filled by the copy engine; tile rows beyond h hold stale data whose
-// accumulator lanes are never stored). Each pipeline stage moves
-// kBoxesPerStage boxes of kBlockK columns: a weight box of h rows (its slot is
-// h rounded up to 8 rows, 1 KiB per 8 rows) and an activation box of 16 rows.
+// accumulator lanes are never stored). Each pipeline stage moves `bps` boxes
+// of kBlockK columns (1 <= bps <= kMaxBoxesPerStage, chosen per launch): a
+// weight box of h rows (its slot is h rounded up to 8 rows, 1 KiB per 8 rows)
+// and an activation box of 16 rows. A stage is one mbarrier round trip between
+// the copy engine and the MMA issuer; with one CTA per SM that round trip, not
+// the bytes, bounds the stream unless stages are large, so the planner makes
+// them as large as the ring allows while keeping at least three in flight.
 constexpr int kMmaM = 128;
 constexpr int kTokTile = 16;
 constexpr int kBlockK = 64;
-constexpr int kBoxesPerStage = 2;
+constexpr int kMaxBoxesPerStage = 8;
 constexpr int kSlotXBytes = kTokTile * kBlockK * 2;  // 2 KiB
 constexpr int kMmaABytes = kMmaM * kBlockK * 2;      // 16 KiB read by one MMA row block
 constexpr int kMaxStages = 16;
-// Independent TMEM accumulators: within a stage, k-step kk of box j goes to
-// accumulator j * 4 + kk, so consecutive MMAs never wait on each other's sum
-// (with one accumulator the MMAs of a 16-token tile run back to back at their
-// full latency). The epilogue adds them in a fixed order.
-constexpr int kNumAcc = kBoxesPerStage * (kBlockK / 16);  // 8
-constexpr int kTmemCols = kNumAcc * kTokTile;             // 128
+// Independent TMEM accumulators: k-step kk of box j of a stage goes to
+// accumulator (j * 4 + kk) mod kNumAcc, so consecutive MMAs never wait on each
+// other's sum (with one accumulator the MMAs of a 16-token tile run back to
+// back at their full latency). Accumulator q is first written by box q / 4 of
+// the slice's first stage; the epilogue adds the used ones in a fixed order.
+constexpr int kNumAcc = 8;
+constexpr int kTmemCols = kNumAcc * kTokTile;  // 128
+__host__ __device__ constexpr int acc_index(int j, int kk) { return (j * 4 + kk) & (kNumAcc - 1); }
+// Accumulators written by a K slice of nkb boxes moved bps per stage.
+__host__ __device__ inline int acc_used(int nkb, int bps) {
+  return (nkb < bps ? nkb : bps) >= 2 ? kNumAcc : kNumAcc / 2;
+}
 // Shared memory per CTA when two CTAs share an SM.
 constexpr size_t kTwoPerSmSmem = 110 * 1024;
 // Shared memory per CTA when one CTA owns an SM.
@@ -51,10 +61,10 @@ struct GemmLayout {
   int total;   // bytes from the aligned base to the end of the flag words
 };
 
-__host__ __device__ inline GemmLayout gemm_layout(int h, int stages) {
+__host__ __device__ inline GemmLayout gemm_layout(int h, int stages, int bps) {
   GemmLayout L;
   L.slot_w = ((h + 7) / 8) * 1024;
-  const int nslot = stages * kBoxesPerStage;
+  const int nslot = stages * bps;
   L.x_off = nslot * L.slot_w;
   int end = L.x_off + nslot * kSlotXBytes;
   const int mma_end = (nslot - 1) * L.slot_w + kMmaABytes;
@@ -76,17 +86,19 @@ struct DeviceInfo {
 // device. Returns cudaSuccess or the first error.
 cudaError_t device_setup(int device, DeviceInfo *info);
 
-// Dynamic shared memory of a GEMM CTA with tile height h and `stages` stages.
-size_t gemm_smem_bytes(int h, int stages);
+// Dynamic shared memory of a GEMM CTA with tile height h and `stages` stages
+// of `bps` boxes.
+size_t gemm_smem_bytes(int h, int stages, int bps);
 
 // Largest number of clusters of `splits` GEMM CTAs that can be resident at
 // once with `ctas_per_sm` (1 or 2) GEMM CTAs per SM (cached).
 int gemm_max_clusters(int device, int splits, int ctas_per_sm);
 
 // Launches the split-K GEMM: grid (ceil(n / h), splits), cluster
-// (1, splits, 1); tile height h rows, `stages` pipeline stages per CTA.
+// (1, splits, 1); tile height h rows, `stages` pipeline stages of `bps` boxes.
 cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, uint16_t *y, int m,
-                        int n, int k, int splits, int h, int stages, cudaStream_t stream, bool pdl);
+                        int n, int k, int splits, int h, int stages, int bps, cudaStream_t stream,
+                        bool pdl);
 
 cudaError_t launch_rmsnorm_nvfp4(const uint16_t *y, const uint16_t *norm_w, float eps, float gc,
                                  const float *gs, uint8_t *a, uint8_t *a_sf, uint16_t *z_out,
@@ -118,7 +130,7 @@ struct DecodeArgs {
   int h[kDecPhases];      // tile rows per phase
   int tiles[kDecPhases];  // CTA c owns tile c of phase p when c < tiles[p]
   int nkb[kDecPhases];    // 64-wide K blocks per phase
-  int stages;
+  int stages, bps;        // pipeline stages, boxes per stage
   int slot_w;             // bytes per weight slot
   const uint16_t *post_w, *beta, *pre_w, *norm_w;
   float alpha, eps_post, eps_pre, gc_post, gc_pre, eps_pool, gc_pool;
@@ -136,9 +148,9 @@ struct DecodeLayout {
   int x_off, bar_off, red_off, total;
 };
 
-__host__ __device__ inline DecodeLayout decode_layout(int slot_w, int stages) {
+__host__ __device__ inline DecodeLayout decode_layout(int slot_w, int stages, int bps) {
   DecodeLayout L;
-  const int nslot = stages * kBoxesPerStage;
+  const int nslot = stages * bps;
   L.x_off = nslot * slot_w;
   int end = L.x_off + nslot * kSlotXBytes;
   const int mma_end = (nslot - 1) * slot_w + kMmaABytes;
@@ -153,7 +165,7 @@ __host__ __device__ inline DecodeLayout decode_layout(int slot_w, int stages) {
 
 cudaError_t launch_decode_layer(const DecodeMaps &maps, const DecodeArgs &args, int grid,
                                 size_t smem, cudaStream_t stream, bool pdl);
-size_t decode_smem_bytes(int slot_w, int stages);
+size_t decode_smem_bytes(int slot_w, int stages, int bps);
 // CTAs of decode_layer_kernel that fit one SM with `smem` bytes.
 int decode_blocks_per_sm(size_t smem);
 

@@ -32,6 +32,7 @@ struct GemmArgs {
   int h;             // weight rows per CTA (tile height), 1..kMmaM
   int kb_per_split;  // kBlockK-wide K blocks per CTA
   int stages;
+  int bps;           // boxes per stage
   int splits;
 };
 
@@ -48,7 +49,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 }
 
 // One CTA = h weight rows x one K slice of kb_per_split * 64 elements, moved
-// kBoxesPerStage 64-column boxes per pipeline stage.
+// args.bps 64-column boxes per pipeline stage.
 // Warp 0 lane 0: TMA producer. Warp 1 lane 0: MMA issuer. Warp 2 owns the
 // TMEM allocation. All four warps run the epilogue (one TMEM lane per thread).
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -57,9 +58,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  constexpr int B = kBoxesPerStage;
+  const int B = args.bps;
   const int stages = args.stages;
-  const GemmLayout lay = gemm_layout(args.h, stages);
+  const GemmLayout lay = gemm_layout(args.h, stages, B);
   const int slot_w = lay.slot_w;
   uint8_t *s_w = smem;                                     // stages*B weight slots
   uint8_t *s_x = smem + lay.x_off;                         // stages*B activation slots
@@ -160,10 +161,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint64_t bdesc = smem_desc_k128(smem_u32(s_x + (s * B + j) * kSlotXBytes));
 #pragma unroll
         for (int kk = 0; kk < kBlockK / 16; ++kk) {
-          // K advances 16 elements = 32 bytes inside the 128-byte swizzle row;
-          // each (box, k-step) of a stage has its own accumulator.
-          tc_mma_bf16(tmem + static_cast<uint32_t>((j * 4 + kk) * kTokTile), adesc + 2 * kk,
-                      bdesc + 2 * kk, kIdesc, i != 0);
+          // K advances 16 elements = 32 bytes inside the 128-byte swizzle row.
+          tc_mma_bf16(tmem + static_cast<uint32_t>(acc_index(j, kk) * kTokTile), adesc + 2 * kk,
+                      bdesc + 2 * kk, kIdesc, i != 0 || j >= kNumAcc / 4);
         }
       }
       tc_commit(empty0 + 8 * s);  // frees the stage once these MMAs have read it
@@ -188,9 +188,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after_sync();
 
   float acc[kTokTile];
-  // accumulators of the second box are used only if the slice has two boxes
   tmem_sum_accumulators<kNumAcc>(tmem + (static_cast<uint32_t>(warp * 32) << 16),
-                                 nkb >= 2 ? kNumAcc : kNumAcc / 2, acc);
+                                 acc_used(nkb, B), acc);
 
   // Outputs may still be read by the previous kernel in the stream.
   griddep_wait();
@@ -536,8 +535,8 @@ __global__ void convert_probe_kernel(int kind, const void *__restrict__ in, void
 namespace sk {
 
 // ---------------------------------------------------------------- host side
-size_t gemm_smem_bytes(int h, int stages) {
-  return 1024 + static_cast<size_t>(gemm_layout(h, stages).total);
+size_t gemm_smem_bytes(int h, int stages, int bps) {
+  return 1024 + static_cast<size_t>(gemm_layout(h, stages, bps).total);
 }
 
 namespace {
@@ -638,8 +637,8 @@ int gemm_max_clusters(int device, int splits, int ctas_per_sm) {
 }
 
 cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, uint16_t *y, int m,
-                        int n, int k, int splits, int h, int stages, cudaStream_t stream,
-                        bool pdl) {
+                        int n, int k, int splits, int h, int stages, int bps,
+                        cudaStream_t stream, bool pdl) {
   GemmArgs a;
   a.y = y;
   a.m = m;
@@ -647,9 +646,10 @@ cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, ui
   a.h = h;
   a.kb_per_split = k / (kBlockK * splits);
   a.stages = stages;
+  a.bps = bps;
   a.splits = splits;
   const dim3 grid((n + h - 1) / h, splits, 1);
-  return launch_ex(gemm_kernel, grid, dim3(kGemmThreads), gemm_smem_bytes(h, stages), stream, pdl,
+  return launch_ex(gemm_kernel, grid, dim3(kGemmThreads), gemm_smem_bytes(h, stages, bps), stream, pdl,
                    dim3(1, splits, 1), tmap_w, tmap_x, a);
 }
 
