@@ -7,6 +7,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <numeric>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -77,17 +78,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D BF16 tensor map over a row-major [rows, cols] matrix, box
-// [box_rows, 64 columns], 128-byte swizzle (the layout the MMA descriptors
-// expect). Rows past `rows` read as zero.
-sk_status make_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows) {
+// Tensor map of a row-major BF16 matrix [rows, cols] seen as three
+// dimensions {64 columns, rows, cols / 64 blocks}: one box is `box_blocks`
+// consecutive 64-column blocks of `box_rows` rows, landing in shared memory as
+// box_blocks tiles of box_rows x 128 bytes, each with the 128-byte swizzle the
+// MMA descriptors expect (box_rows a multiple of 8 keeps every tile 1 KiB
+// aligned). Rows past `rows` and blocks past cols / 64 read as zero.
+sk_status make_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows,
+                   int box_blocks) {
   auto fn = encode_fn();
   if (!fn) return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(sk::kBlockK), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(sk::kBlockK), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(cols / sk::kBlockK)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, sk::kBlockK * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(sk::kBlockK), static_cast<cuuint32_t>(box_rows),
+                       static_cast<cuuint32_t>(box_blocks)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
@@ -131,7 +138,7 @@ template <typename Bytes>
 void choose_ring(int nkb, size_t budget, Bytes bytes, int *stages, int *bps) {
   int best_b = 1;
   for (int b = sk::kMaxBoxesPerStage; b >= 1; --b) {
-    if (b > nkb && b > 1) continue;
+    if (b > 1 && nkb % b) continue;  // whole stages: a box never reads past the slice
     const int need = std::min(3, (nkb + b - 1) / b);
     if (bytes(need, b) <= budget) {
       best_b = b;
@@ -184,6 +191,7 @@ GemmPlan plan_gemm(int n, int k, int splits_req, int device, int sm_count) {
     p.h = h < 16 ? 16 : (h > sk::kMmaM ? sk::kMmaM : h);
   }
   if (const int hv = env_int("SK_TILE_ROWS", 16, sk::kMmaM)) p.h = hv;
+  p.h = (p.h + 7) / 8 * 8;  // whole 8-row swizzle atoms per 64-column block
   const int tiles = (n + p.h - 1) / p.h;
   const size_t budget = tiles * p.splits <= sm_count ? sk::kOnePerSmSmem : sk::kTwoPerSmSmem;
   choose_ring(nkb_total / p.splits, budget,
@@ -208,8 +216,8 @@ sk_status enqueue_gemm(const void *x, const void *w, void *y, int m, int n, int 
     return fail(SK_ERR_UNSUPPORTED, "no GEMM launch for n=%d, k=%d, splits=%d", n, k, splits);
   CUtensorMap tw, tx;
   sk_status st;
-  if ((st = make_map(&tw, w, n, k, plan.h)) != SK_OK) return st;
-  if ((st = make_map(&tx, x, m, k, sk::kTokTile)) != SK_OK) return st;
+  if ((st = make_map(&tw, w, n, k, plan.h, plan.bps)) != SK_OK) return st;
+  if ((st = make_map(&tx, x, m, k, sk::kTokTile, plan.bps)) != SK_OK) return st;
   return launch_status(sk::launch_gemm(tw, tx, static_cast<uint16_t *>(y), m, n, k, plan.splits,
                                        plan.h, plan.stages, plan.bps, as_stream(stream),
                                        pdl_enabled()),
@@ -233,10 +241,6 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 }  // namespace
 
 sk_status sk::report_error(sk_status st, const char *msg) { return fail(st, "%s", msg); }
-
-sk_status sk::make_tensor_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows) {
-  return make_map(map, base, rows, cols, box_rows);
-}
 
 sk_status sk::checked_device(sk::DeviceInfo *info, int *device) {
   sk_status st = current_device(info);
@@ -461,8 +465,9 @@ sk_status sk_decode_layer(const void *h_in, const void *w_o, const void *w_p, co
   const int ks[3] = {k_oproj, hidden, pooled};
   int slot_w = 0;
   for (int p = 0; p < 3; ++p) {
+    // whole 8-row swizzle atoms; the pooler's tiles hold whole NVFP4 blocks
     int h = (rows[p] + G - 1) / G;
-    if (p == 1) h = (h + 15) / 16 * 16;
+    h = p == 1 ? (h + 15) / 16 * 16 : (h + 7) / 8 * 8;
     if (h > sk::kMmaM)
       return fail(SK_ERR_UNSUPPORTED, "%d rows need more than %d rows per CTA on %d SMs", rows[p],
                   sk::kMmaM, G);
@@ -474,14 +479,16 @@ sk_status sk_decode_layer(const void *h_in, const void *w_o, const void *w_p, co
   }
   args.slot_w = slot_w;
   const size_t cap = info.max_smem_optin - 1024;
-  const int nkb_max = std::max(args.nkb[0], std::max(args.nkb[1], args.nkb[2]));
-  choose_ring(nkb_max, cap, [&](int s, int b) { return sk::decode_smem_bytes(slot_w, s, b); },
+  // a stage size that divides every phase's K blocks
+  const int nkb_all = std::gcd(args.nkb[0], std::gcd(args.nkb[1], args.nkb[2]));
+  choose_ring(nkb_all, cap, [&](int s, int b) { return sk::decode_smem_bytes(slot_w, s, b); },
               &args.stages, &args.bps);
   // the ring serves every phase in turn: keep all of its stages
   while (args.stages < sk::kMaxStages &&
          sk::decode_smem_bytes(slot_w, args.stages + 1, args.bps) <= cap)
     ++args.stages;
   const size_t smem = sk::decode_smem_bytes(slot_w, args.stages, args.bps);
+  args.rotate = sk::rotate_k_order();
   if (sk::decode_blocks_per_sm(smem) < 1)
     return fail(SK_ERR_UNSUPPORTED, "the fused layer kernel cannot be resident with %zu bytes", smem);
   args.post_w = static_cast<const uint16_t *>(post_w);
@@ -514,8 +521,8 @@ sk_status sk_decode_layer(const void *h_in, const void *w_o, const void *w_p, co
   const void *xs[3] = {h_in, u_out, z_out};
   const int xcols[3] = {k_oproj, hidden, pooled};
   for (int p = 0; p < 3; ++p) {
-    if ((st = make_map(&maps.w[p], wts[p], rows[p], ks[p], args.h[p])) != SK_OK) return st;
-    if ((st = make_map(&maps.x[p], xs[p], m, xcols[p], sk::kTokTile)) != SK_OK) return st;
+    if ((st = make_map(&maps.w[p], wts[p], rows[p], ks[p], args.h[p], args.bps)) != SK_OK) return st;
+    if ((st = make_map(&maps.x[p], xs[p], m, xcols[p], sk::kTokTile, args.bps)) != SK_OK) return st;
   }
   cudaError_t e = cudaMemsetAsync(workspace, 0, 256, as_stream(stream));
   if (e != cudaSuccess) return fail(SK_ERR_CUDA, "workspace clear failed: %s", cudaGetErrorString(e));

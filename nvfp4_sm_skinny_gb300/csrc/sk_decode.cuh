@@ -10,10 +10,12 @@
 // while the ring keeps filling. Separate kernels would drain and refill the
 // memory pipeline at every boundary.
 //
-// Roles (192 threads): warp 0 lane 0 issues the TMA copies (weights as soon as
-// a ring slot is free; activations once the step's input is complete), warp 1
-// lane 0 issues the tcgen05 MMAs, warps 2-5 (one per TMEM lane quadrant) run
-// the epilogues: dual norm, RMSNorm + NVFP4, stores. The arithmetic of each
+// Roles (kDecThreads threads): warp 0 lane 0 issues the TMA copies (weights
+// as soon as a ring slot is free; activations once the step's input is
+// complete), lane 0 of warps 1..kDecIssuers issue the tcgen05 MMAs (box j of a
+// stage to issuer j mod kDecIssuers, each with its own accumulators), and the
+// last four warps (one per TMEM lane quadrant) run the epilogues: dual norm,
+// RMSNorm + NVFP4, stores. The arithmetic of each
 // epilogue matches the standalone kernels (same FP32 operations per element;
 // reductions in a fixed order), so results are bitwise reproducible run to run.
 //
@@ -174,20 +176,23 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const uint32_t done0 = smem_u32(bars + 2 * S);
 
   // stage sequence of this CTA: the phases it has a tile in, in order
-  int nst[kDecPhases], st0[kDecPhases], total = 0;
+  int nst[kDecPhases], st0[kDecPhases], rot[kDecPhases], total = 0;
 #pragma unroll
   for (int p = 0; p < kDecPhases; ++p) {
     nst[p] = c < args.tiles[p] ? (args.nkb[p] + B - 1) / B : 0;
     st0[p] = total;
     total += nst[p];
+    rot[p] = args.rotate ? stage_rotation(c, args.tiles[p], nst[p]) : 0;
   }
+  // first 64-wide K block of stage ls of phase p
+  auto kb_of = [&](int ls, int p) { return rotated_stage(ls, rot[p], nst[p]) * B; };
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 2);  // the weight arrival and the activation arrival
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kDecIssuers);
     }
-    for (int p = 0; p < kDecPhases; ++p) mbar_init(done0 + 8 * p, 1);
+    for (int p = 0; p < kDecPhases; ++p) mbar_init(done0 + 8 * p, kDecIssuers);
     *abort_flag = 0;
     x_ready[0] = 0;
     x_ready[1] = 0;
@@ -198,7 +203,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_alloc(smem_u32(tmem_slot), kDecTmemCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
@@ -219,7 +224,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         while (p + 1 < kDecPhases && i >= st0[p + 1]) ++p;
         return p;
       };
-      auto nb_of = [&](int i, int p) { return min(B, args.nkb[p] - (i - st0[p]) * B); };
       // activation copies of armed stages whose input is complete
       auto issue_x = [&](int armed) {
         while (xi < armed) {
@@ -230,20 +234,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             fence_proxy_async_global();  // generic-proxy stores of other CTAs -> TMA reads
             ready[p] = true;
           }
-          const int s = xi % S, nb = nb_of(xi, p);
-          mbar_arrive_expect_tx(full0 + 8 * s, nb * kSlotXBytes);
-          for (int j = 0; j < nb; ++j)
-            tma_load_2d(smem_u32(s_x + (s * B + j) * kSlotXBytes), &maps.x[p], full0 + 8 * s,
-                        ((xi - st0[p]) * B + j) * kBlockK, 0, pol_x);
+          const int s = xi % S;
+          mbar_arrive_expect_tx(full0 + 8 * s, B * kSlotXBytes);
+          tma_load_3d(smem_u32(s_x + s * B * kSlotXBytes), &maps.x[p], full0 + 8 * s, 0, 0,
+                      kb_of(xi - st0[p], p), pol_x);
           ++xi;
         }
       };
       auto arm_w = [&](int i) {
-        const int p = phase_of(i), s = i % S, nb = nb_of(i, p);
-        mbar_arrive_expect_tx(full0 + 8 * s, nb * args.h[p] * 128);
-        for (int j = 0; j < nb; ++j)
-          tma_load_2d(smem_u32(s_w + (s * B + j) * slot_w), &maps.w[p], full0 + 8 * s,
-                      ((i - st0[p]) * B + j) * kBlockK, c * args.h[p], pol_w);
+        const int p = phase_of(i), s = i % S;
+        // one copy: B blocks of h[p] rows (blocks past K arrive as zeros)
+        mbar_arrive_expect_tx(full0 + 8 * s, B * args.h[p] * 128);
+        tma_load_3d(smem_u32(s_w + s * B * slot_w), &maps.w[p], full0 + 8 * s, 0, c * args.h[p],
+                    kb_of(i - st0[p], p), pol_w);
       };
       const int fill = total < S ? total : S;
       for (int i = 0; i < fill; ++i) arm_w(i);  // weights first: never written by a kernel
@@ -285,27 +288,31 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         __nanosleep(128);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp <= kDecIssuers) {
     if (lane == 0) {
-      // ------------------------------------------------------ MMA issuer
+      // ------------------------------------------------------ MMA issuers
+      const int q = warp - 1;
       int i = 0;
       bool ok = true;
       for (int p = 0; p < kDecPhases && ok; ++p) {
         if (nst[p] == 0) continue;
+        bool started = false;  // this issuer's accumulators hold this phase's partial sum
         for (int ls = 0; ls < nst[p]; ++ls, ++i) {
           const int s = i % S;
           const uint32_t par = (i / S) & 1;
           if (!dec_wait(full0 + 8 * s, par, abort_flag, args.gabort, SK_DEVICE_WAIT_MMA)) ok = false;
           if (!ok) break;
           tc_fence_after_sync();
-          const int nb = min(B, args.nkb[p] - ls * B);
-          for (int j = 0; j < nb; ++j) {
-            const uint64_t adesc = smem_desc_k128(smem_u32(s_w + (s * B + j) * slot_w));
+          const int nb = min(B, args.nkb[p] - kb_of(ls, p));
+          for (int j = q; j < nb; j += kDecIssuers) {
+            // block j of the stage: h[p] rows of 128 bytes after block j - 1
+            const uint64_t adesc = smem_desc_k128(smem_u32(s_w + s * B * slot_w + j * args.h[p] * 128));
             const uint64_t bdesc = smem_desc_k128(smem_u32(s_x + (s * B + j) * kSlotXBytes));
 #pragma unroll
             for (int kk = 0; kk < kBlockK / 16; ++kk)
-              tc_mma_bf16(tmem + static_cast<uint32_t>(acc_index(j, kk) * kTokTile), adesc + 2 * kk,
-                          bdesc + 2 * kk, kIdesc, ls != 0 || j >= kNumAcc / 4);
+              tc_mma_bf16(tmem + static_cast<uint32_t>(acc_index(q, kk) * kTokTile), adesc + 2 * kk,
+                          bdesc + 2 * kk, kIdesc, started);
+            started = true;
           }
           tc_commit(empty0 + 8 * s);
         }
@@ -317,7 +324,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
   } else {
     // -------------------------------------------------------- epilogue
-    const int ew = warp - 2;                      // 0..3
+    const int ew = warp - 1 - kDecIssuers;        // 0..3
     const int e = ((warp & 3) << 5) + lane;       // TMEM lane = tile row
     const int m = args.m, H = args.H, P = args.P;
     const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
@@ -347,7 +354,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         atomicExch(args.gabort, 1u);
       }
       tc_fence_after_sync();
-      tmem_sum_accumulators<kNumAcc>(taddr, acc_used(args.nkb[0], B), v);
+      tmem_sum_accumulators<kDecNumAcc>(taddr, acc_used(args.nkb[0], B, kDecIssuers), v);
       tc_fence_before_sync();
 #pragma unroll
       for (int t = 0; t < 16; ++t) pv[t] = (valid0 && t < m) ? bf16_round_f32(v[t]) : 0.0f;
@@ -406,7 +413,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         atomicExch(args.gabort, 1u);
       }
       tc_fence_after_sync();
-      tmem_sum_accumulators<kNumAcc>(taddr, acc_used(args.nkb[1], B), v);
+      tmem_sum_accumulators<kDecNumAcc>(taddr, acc_used(args.nkb[1], B, kDecIssuers), v);
       tc_fence_before_sync();
 #pragma unroll
       for (int t = 0; t < 16; ++t) yv[t] = (valid1 && t < m) ? bf16_round_f32(v[t]) : 0.0f;
@@ -467,7 +474,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         atomicExch(args.gabort, 1u);
       }
       tc_fence_after_sync();
-      tmem_sum_accumulators<kNumAcc>(taddr, acc_used(args.nkb[2], B), v);
+      tmem_sum_accumulators<kDecNumAcc>(taddr, acc_used(args.nkb[2], B, kDecIssuers), v);
       tc_fence_before_sync();
       if (e < h2 && n2 < H && !*abort_flag) {
 #pragma unroll
@@ -487,7 +494,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
   }
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, kDecTmemCols);
 }
 
 cudaError_t launch_decode_layer(const DecodeMaps &maps, const DecodeArgs &args, int grid,

@@ -32,17 +32,37 @@ constexpr int kMaxBoxesPerStage = 8;
 constexpr int kSlotXBytes = kTokTile * kBlockK * 2;  // 2 KiB
 constexpr int kMmaABytes = kMmaM * kBlockK * 2;      // 16 KiB read by one MMA row block
 constexpr int kMaxStages = 16;
-// Independent TMEM accumulators: k-step kk of box j of a stage goes to
-// accumulator (j * 4 + kk) mod kNumAcc, so consecutive MMAs never wait on each
-// other's sum (with one accumulator the MMAs of a 16-token tile run back to
-// back at their full latency). Accumulator q is first written by box q / 4 of
-// the slice's first stage; the epilogue adds the used ones in a fixed order.
-constexpr int kNumAcc = 8;
-constexpr int kTmemCols = kNumAcc * kTokTile;  // 128
-__host__ __device__ constexpr int acc_index(int j, int kk) { return (j * 4 + kk) & (kNumAcc - 1); }
-// Accumulators written by a K slice of nkb boxes moved bps per stage.
-__host__ __device__ inline int acc_used(int nkb, int bps) {
-  return (nkb < bps ? nkb : bps) >= 2 ? kNumAcc : kNumAcc / 2;
+// MMA issue. One thread issuing tcgen05.mma is held for a fixed time per
+// instruction whatever its M and N (measured on GB300: ~75 ns), which at
+// 128 x 16 x 16 caps one issuer at ~55 GB/s of weight; the rate grows with the
+// number of issuing warps per SM. So a CTA issues from several warps: box j of
+// a stage goes to issuer j mod NI, and issuer q's k-step kk accumulates into
+// its own TMEM accumulator q * 4 + kk (16 FP32 columns), first written by the
+// issuer's first box of the slice. The epilogue adds the used accumulators in
+// index order, so the sum order is fixed.
+constexpr int kGemmIssuers = 2;
+constexpr int kNumAcc = kGemmIssuers * (kBlockK / 16);  // 8
+constexpr int kTmemCols = kNumAcc * kTokTile;           // 128
+__host__ __device__ constexpr int acc_index(int q, int kk) { return q * (kBlockK / 16) + kk; }
+// Accumulators written by a K slice of nkb boxes moved bps per stage by ni
+// issuers: those of the issuers that own a box of the first stage.
+__host__ __device__ inline int acc_used(int nkb, int bps, int ni) {
+  int b = nkb < bps ? nkb : bps;
+  if (b > ni) b = ni;
+  return b * (kBlockK / 16);
+}
+// K order. Every CTA of a row of tiles reads the same activation boxes; walked
+// in lockstep from k = 0, all of them would ask the same few L2 lines for the
+// same box at once and queue on them. So tile r of G walks its nst stages
+// starting at stage rot = floor(r * nst / G) and wraps around: at any moment
+// the CTAs spread their activation reads over the whole of x. The order is
+// fixed by the launch shape, so results stay bitwise reproducible.
+__host__ __device__ inline int stage_rotation(int r, int G, int nst) {
+  return nst > 1 ? static_cast<int>((static_cast<long long>(r) * nst) / G) % nst : 0;
+}
+__host__ __device__ inline int rotated_stage(int i, int rot, int nst) {
+  const int v = i + rot;
+  return v >= nst ? v - nst : v;
 }
 // Shared memory per CTA when two CTAs share an SM.
 constexpr size_t kTwoPerSmSmem = 110 * 1024;
@@ -100,6 +120,9 @@ cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, ui
                         int n, int k, int splits, int h, int stages, int bps, cudaStream_t stream,
                         bool pdl);
 
+// 1 unless the environment sets SK_ROTATE=0: stagger the K order of row tiles.
+int rotate_k_order();
+
 cudaError_t launch_rmsnorm_nvfp4(const uint16_t *y, const uint16_t *norm_w, float eps, float gc,
                                  const float *gs, uint8_t *a, uint8_t *a_sf, uint16_t *z_out,
                                  int m, int n, cudaStream_t stream, bool pdl);
@@ -117,7 +140,14 @@ cudaError_t launch_convert_probe(int kind, const void *in, void *out, int n, cud
 cudaError_t read_device_status(uint32_t *out, bool clear);
 
 // Fused decode layer (sk_decode.cuh): arguments, layout, launch.
-constexpr int kDecThreads = 192;
+// Warp 0: TMA producer; warps 1..kDecIssuers: MMA issuers (tile rows are
+// fewer than 128 here, so each instruction carries less weight and more
+// issuers are needed); the last four warps: epilogue, one per TMEM lane
+// quadrant.
+constexpr int kDecIssuers = 4;
+constexpr int kDecThreads = 32 * (1 + kDecIssuers + 4);
+constexpr int kDecNumAcc = kDecIssuers * (kBlockK / 16);  // 16
+constexpr int kDecTmemCols = kDecNumAcc * kTokTile;       // 256
 constexpr int kDecPhases = 3;  // 0: o_proj, 1: pooler, 2: unpooler
 
 struct DecodeMaps {
@@ -131,6 +161,7 @@ struct DecodeArgs {
   int tiles[kDecPhases];  // CTA c owns tile c of phase p when c < tiles[p]
   int nkb[kDecPhases];    // 64-wide K blocks per phase
   int stages, bps;        // pipeline stages, boxes per stage
+  int rotate;             // 1: stagger the K order across tiles
   int slot_w;             // bytes per weight slot
   const uint16_t *post_w, *beta, *pre_w, *norm_w;
   float alpha, eps_post, eps_pre, gc_post, gc_pre, eps_pool, gc_pool;
@@ -169,10 +200,6 @@ size_t decode_smem_bytes(int slot_w, int stages, int bps);
 // CTAs of decode_layer_kernel that fit one SM with `smem` bytes.
 int decode_blocks_per_sm(size_t smem);
 
-// Host helpers shared by the entry points (defined in sk_api.cu).
-// 2-D BF16 tensor map over a row-major [rows, cols] matrix, box [box_rows, 64
-// columns], 128-byte swizzle; rows past `rows` read as zero.
-sk_status make_tensor_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows);
 // The current device, checked to be compute capability 10.3, set up.
 sk_status checked_device(DeviceInfo *info, int *device);
 bool pdl_on();

@@ -34,6 +34,7 @@ struct GemmArgs {
   int stages;
   int bps;           // boxes per stage
   int splits;
+  int rotate;        // 1: stagger the K order across row tiles
 };
 
 // Bounded wait that also gives up as soon as another role raised `abort`.
@@ -50,8 +51,9 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 
 // One CTA = h weight rows x one K slice of kb_per_split * 64 elements, moved
 // args.bps 64-column boxes per pipeline stage.
-// Warp 0 lane 0: TMA producer. Warp 1 lane 0: MMA issuer. Warp 2 owns the
-// TMEM allocation. All four warps run the epilogue (one TMEM lane per thread).
+// Warp 0 lane 0: TMA producer. Lane 0 of warps 1..kGemmIssuers: MMA issuers.
+// Warp 2 owns the TMEM allocation. All four warps run the epilogue (one TMEM
+// lane per thread).
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                 GemmArgs args) {
@@ -74,7 +76,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int nkb = args.kb_per_split;
   const int kb0 = blockIdx.y * nkb;
   const int nst = (nkb + B - 1) / B;                     // pipeline stages of work
-  const uint32_t box_tx = static_cast<uint32_t>(h * 128 + kSlotXBytes);
+  const int rot = args.rotate ? stage_rotation(blockIdx.x, gridDim.x, nst) : 0;
+  const uint32_t stage_tx = static_cast<uint32_t>(B * (h * 128 + kSlotXBytes));
 
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = smem_u32(bars + stages);
@@ -83,9 +86,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kGemmIssuers);  // one commit per issuer
     }
-    mbar_init(done_bar, 1);
+    mbar_init(done_bar, kGemmIssuers);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_map(&tmap_w);
@@ -110,22 +113,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint64_t pol_w = l2_policy_evict_first();  // the weight is streamed once
     const uint64_t pol_x = l2_policy_evict_last();   // x is re-read by every row tile
     const int npre = nst < stages ? nst : stages;
+    // One copy per operand and stage: the weight box is B blocks of h rows, the
+    // activation box B blocks of 16 token rows (rows past m and blocks past K
+    // arrive as zeros and count toward the transaction bytes all the same).
     // The weight is never written by another kernel: fill the ring with it
     // before waiting for the previous kernel in the stream.
     for (int i = 0; i < npre; ++i) {
-      const int nb = min(B, nkb - i * B);
-      mbar_arrive_expect_tx(full0 + 8 * i, nb * box_tx);
-      for (int j = 0; j < nb; ++j)
-        tma_load_2d(smem_u32(s_w + (i * B + j) * slot_w), &tmap_w, full0 + 8 * i,
-                    (kb0 + i * B + j) * kBlockK, n0, pol_w);
+      mbar_arrive_expect_tx(full0 + 8 * i, stage_tx);
+      tma_load_3d(smem_u32(s_w + i * B * slot_w), &tmap_w, full0 + 8 * i, 0, n0,
+                  kb0 + rotated_stage(i, rot, nst) * B, pol_w);
     }
     griddep_wait();
-    for (int i = 0; i < npre; ++i) {
-      const int nb = min(B, nkb - i * B);
-      for (int j = 0; j < nb; ++j)
-        tma_load_2d(smem_u32(s_x + (i * B + j) * kSlotXBytes), &tmap_x, full0 + 8 * i,
-                    (kb0 + i * B + j) * kBlockK, 0, pol_x);
-    }
+    for (int i = 0; i < npre; ++i)
+      tma_load_3d(smem_u32(s_x + i * B * kSlotXBytes), &tmap_x, full0 + 8 * i, 0, 0,
+                  kb0 + rotated_stage(i, rot, nst) * B, pol_x);
     issued = npre;
     for (int i = npre; i < nst; ++i) {
       const int s = i % stages;
@@ -135,17 +136,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         *abort_flag = 1;
         break;
       }
-      const int nb = min(B, nkb - i * B);
-      mbar_arrive_expect_tx(full0 + 8 * s, nb * box_tx);
-      for (int j = 0; j < nb; ++j) {
-        const int kc = (kb0 + i * B + j) * kBlockK;
-        tma_load_2d(smem_u32(s_w + (s * B + j) * slot_w), &tmap_w, full0 + 8 * s, kc, n0, pol_w);
-        tma_load_2d(smem_u32(s_x + (s * B + j) * kSlotXBytes), &tmap_x, full0 + 8 * s, kc, 0, pol_x);
-      }
+      const int kb = kb0 + rotated_stage(i, rot, nst) * B;
+      mbar_arrive_expect_tx(full0 + 8 * s, stage_tx);
+      tma_load_3d(smem_u32(s_w + s * B * slot_w), &tmap_w, full0 + 8 * s, 0, n0, kb, pol_w);
+      tma_load_3d(smem_u32(s_x + s * B * kSlotXBytes), &tmap_x, full0 + 8 * s, 0, 0, kb, pol_x);
       issued = i + 1;
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------------------------------------------- MMA issuer
+  } else if (warp >= 1 && warp <= kGemmIssuers && lane == 0) {
+    // ---------------------------------------------------- MMA issuers
+    const int q = warp - 1;
+    bool started = false;  // this issuer's accumulators hold a partial sum
     for (int i = 0; i < nst; ++i) {
       const int s = i % stages;
       const uint32_t par = (i / stages) & 1;
@@ -155,20 +155,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const int nb = min(B, nkb - i * B);
-      for (int j = 0; j < nb; ++j) {
+      const int nb = min(B, nkb - rotated_stage(i, rot, nst) * B);
+      for (int j = q; j < nb; j += kGemmIssuers) {
         const uint64_t adesc = smem_desc_k128(smem_u32(s_w + (s * B + j) * slot_w));
         const uint64_t bdesc = smem_desc_k128(smem_u32(s_x + (s * B + j) * kSlotXBytes));
 #pragma unroll
         for (int kk = 0; kk < kBlockK / 16; ++kk) {
           // K advances 16 elements = 32 bytes inside the 128-byte swizzle row.
-          tc_mma_bf16(tmem + static_cast<uint32_t>(acc_index(j, kk) * kTokTile), adesc + 2 * kk,
-                      bdesc + 2 * kk, kIdesc, i != 0 || j >= kNumAcc / 4);
+          tc_mma_bf16(tmem + static_cast<uint32_t>(acc_index(q, kk) * kTokTile), adesc + 2 * kk,
+                      bdesc + 2 * kk, kIdesc, started);
         }
+        started = true;
       }
-      tc_commit(empty0 + 8 * s);  // frees the stage once these MMAs have read it
+      tc_commit(empty0 + 8 * s);  // this issuer's share of the stage has been read
     }
-    tc_commit(done_bar);  // accumulator complete (or, after an abort, quiescent)
+    tc_commit(done_bar);  // accumulators complete (or, after an abort, quiescent)
   }
   __syncwarp();
 
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   float acc[kTokTile];
   tmem_sum_accumulators<kNumAcc>(tmem + (static_cast<uint32_t>(warp * 32) << 16),
-                                 acc_used(nkb, B), acc);
+                                 acc_used(nkb, B, kGemmIssuers), acc);
 
   // Outputs may still be read by the previous kernel in the stream.
   griddep_wait();
@@ -636,9 +637,16 @@ int gemm_max_clusters(int device, int splits, int ctas_per_sm) {
   return cache[device][idx][per];
 }
 
+// Staggered K order across row tiles: on unless SK_ROTATE=0 (for comparison).
+int rotate_k_order() {
+  const char *v = std::getenv("SK_ROTATE");
+  return (v && v[0] == '0') ? 0 : 1;
+}
+
 cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, uint16_t *y, int m,
                         int n, int k, int splits, int h, int stages, int bps,
                         cudaStream_t stream, bool pdl) {
+  if (h % 8 || h < 8 || h > kMmaM || bps < 1 || bps > kMaxBoxesPerStage) return cudaErrorInvalidValue;
   GemmArgs a;
   a.y = y;
   a.m = m;
@@ -648,6 +656,7 @@ cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, ui
   a.stages = stages;
   a.bps = bps;
   a.splits = splits;
+  a.rotate = rotate_k_order();
   const dim3 grid((n + h - 1) / h, splits, 1);
   return launch_ex(gemm_kernel, grid, dim3(kGemmThreads), gemm_smem_bytes(h, stages, bps), stream, pdl,
                    dim3(1, splits, 1), tmap_w, tmap_x, a);
