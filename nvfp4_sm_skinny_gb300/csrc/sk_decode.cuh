@@ -72,10 +72,20 @@ __device__ __forceinline__ void epi_grid_sum16(const float *part, int G, float *
   const int c0 = j * chunk, c1 = min(G, c0 + chunk);
   float acc = 0.0f;
   bool first = true;
-  for (int c = c0; c < c1; ++c) {
-    const float v = __ldcg(part + c * 16 + t);
-    acc = first ? v : acc + v;
-    first = false;
+  // all loads of a batch are issued before the first add: one L2 round trip
+  // per batch instead of one per CTA
+  constexpr int kBatch = 24;
+  for (int cb = c0; cb < c1; cb += kBatch) {
+    float v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) v[u] = cb + u < c1 ? __ldcg(part + (cb + u) * 16 + t) : 0.0f;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (cb + u < c1) {
+        acc = first ? v[u] : acc + v[u];
+        first = false;
+      }
+    }
   }
   // the eight chunk sums of token t sit in eight consecutive lanes
   float total = 0.0f;
@@ -104,7 +114,7 @@ __device__ __forceinline__ bool epi_grid_sync(unsigned *bar, unsigned target, un
     atomicAdd(bar, 1u);
     const uint64_t t0 = globaltimer_ns();
     while (ld_acquire_u32(bar) < target) {
-      __nanosleep(256);
+      __nanosleep(32);
       if (*abort_flag || ld_volatile_u32(gabort)) {
         ok = 0;
         break;
@@ -116,7 +126,8 @@ __device__ __forceinline__ bool epi_grid_sync(unsigned *bar, unsigned target, un
         break;
       }
     }
-    __threadfence();
+    // the acquire load that saw the final count orders this CTA's later reads
+    // after every CTA's release (fence + add) of its partials
     if (ok && ready_flag) *ready_flag = 1;
     if (!ok) *abort_flag = 1;
     ok_s = ok;
@@ -431,14 +442,23 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
     if (ok) {
       epi_grid_sum16(args.part + 2 * G * 16, G, tot, ew, lane);
+      // the RMS factor of each token, once per CTA
+      const int et = ew * 32 + lane;
+      if (et < 16)
+        tot[et] = __fdiv_rn(
+            1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot[et], static_cast<float>(P)), args.eps_pool)));
+      epi_bar();
       if (has1 && (e & ~31) < h1) {
         // rows of a 16-column NVFP4 block sit in 16 consecutive lanes (h1 is a
         // multiple of 16, so a block is wholly inside or outside the tile);
-        // every lane of a warp that holds tile rows takes part in the shuffles
+        // every lane of a warp that holds tile rows takes part in the shuffles.
+        // Unrolled over the tokens so that independent tokens overlap.
         const float gs = *args.gs;
-        for (int t = 0; t < m; ++t) {
-          const float rr = __fdiv_rn(
-              1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot[t], static_cast<float>(P)), args.eps_pool)));
+        const float inv_gs = __fdiv_rn(1.0f, gs);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          if (t >= m) break;
+          const float rr = tot[t];
           const uint16_t zb = valid1 ? bf16_store_bits(__fmul_rn(__fmul_rn(yv[t], rr), gv)) : 0;
           const float zf = bf16_bits_to_f32(zb);
           float amax = fabsf(zf);
@@ -448,7 +468,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           const float tq = __fmul_rn(__fdiv_rn(amax, 6.0f), gs);
           const uint32_t sf = cvt_f32_e4m3(tq);
           const float sff = cvt_e4m3_f32(sf);
-          const float os = (sff == 0.0f) ? 0.0f : __fdiv_rn(1.0f, __fmul_rn(sff, __fdiv_rn(1.0f, gs)));
+          const float os = (sff == 0.0f) ? 0.0f : __fdiv_rn(1.0f, __fmul_rn(sff, inv_gs));
           const float vq = __fmul_rn(zf, os);
           const float vn = __shfl_xor_sync(0xffffffffu, vq, 1);
           if (valid1) {
