@@ -195,7 +195,7 @@ GemmPlan plan_gemm(int n, int k, int splits_req, int device, int sm_count) {
   const int tiles = (n + p.h - 1) / p.h;
   const size_t budget = tiles * p.splits <= sm_count ? sk::kOnePerSmSmem : sk::kTwoPerSmSmem;
   choose_ring(nkb_total / p.splits, budget,
-              [&](int st, int b) { return sk::gemm_smem_bytes(p.h, st, b); }, &p.stages, &p.bps);
+              [&](int st, int b) { return sk::gemm_smem_bytes(p.h, st, b, p.splits); }, &p.stages, &p.bps);
   return p;
 }
 

@@ -67,32 +67,34 @@ __host__ __device__ inline int rotated_stage(int i, int rot, int nst) {
 // Shared memory per CTA when two CTAs share an SM.
 constexpr size_t kTwoPerSmSmem = 110 * 1024;
 // Shared memory per CTA when one CTA owns an SM.
-constexpr size_t kOnePerSmSmem = 220 * 1024;
+constexpr size_t kOnePerSmSmem = 226 * 1024;
 
 // Shared-memory layout of a GEMM CTA, relative to its 1024-aligned base:
-// weight slots [0, w_end), activation slots [x_off, x_end), barriers at
-// bar_off. The data region also covers the 16 KiB an MMA reads from the last
-// weight slot and the split-K partials the ranks push into the ring after the
-// loop (16 tokens x (h + S) rows of FP32 at most).
+// weight slots [0, x_off), activation slots [x_off, red_off) (the data region
+// also covers the 16 KiB an MMA reads from the last weight slot), the split-K
+// exchange buffer [red_off, bar_off) that peers of the cluster write into
+// while this CTA may still be streaming (S ranks x R rows x 16 tokens FP32,
+// R = ceil(h / S)), then the mbarriers.
 struct GemmLayout {
   int slot_w;  // bytes per weight slot
   int x_off;   // first activation slot
-  int bar_off; // mbarriers (2 * stages + 1), then the TMEM address and a flag
+  int red_off; // split-K exchange buffer
+  int bar_off; // mbarriers (2 * stages + 2), then the TMEM address and a flag
   int total;   // bytes from the aligned base to the end of the flag words
 };
 
-__host__ __device__ inline GemmLayout gemm_layout(int h, int stages, int bps) {
+__host__ __device__ inline GemmLayout gemm_layout(int h, int stages, int bps, int splits) {
   GemmLayout L;
   L.slot_w = ((h + 7) / 8) * 1024;
   const int nslot = stages * bps;
   L.x_off = nslot * L.slot_w;
   int end = L.x_off + nslot * kSlotXBytes;
   const int mma_end = (nslot - 1) * L.slot_w + kMmaABytes;
-  const int red_end = kTokTile * (kMmaM + 16) * 4;  // split-K partials, all ranks
   if (mma_end > end) end = mma_end;
-  if (red_end > end) end = red_end;
-  L.bar_off = (end + 7) / 8 * 8;
-  L.total = L.bar_off + (2 * stages + 1) * 8 + 8;
+  L.red_off = (end + 15) / 16 * 16;
+  const int rows = splits > 1 ? splits * ((h + splits - 1) / splits) : 0;
+  L.bar_off = L.red_off + rows * kTokTile * 4;
+  L.total = L.bar_off + (2 * stages + 2) * 8 + 8;
   return L;
 }
 
@@ -106,9 +108,9 @@ struct DeviceInfo {
 // device. Returns cudaSuccess or the first error.
 cudaError_t device_setup(int device, DeviceInfo *info);
 
-// Dynamic shared memory of a GEMM CTA with tile height h and `stages` stages
-// of `bps` boxes.
-size_t gemm_smem_bytes(int h, int stages, int bps);
+// Dynamic shared memory of a GEMM CTA with tile height h, `stages` stages of
+// `bps` boxes and `splits` cluster ranks.
+size_t gemm_smem_bytes(int h, int stages, int bps, int splits);
 
 // Largest number of clusters of `splits` GEMM CTAs that can be resident at
 // once with `ctas_per_sm` (1 or 2) GEMM CTAs per SM (cached).

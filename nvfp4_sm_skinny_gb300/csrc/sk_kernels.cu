@@ -62,12 +62,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int B = args.bps;
   const int stages = args.stages;
-  const GemmLayout lay = gemm_layout(args.h, stages, B);
+  const int S = args.splits;
+  const GemmLayout lay = gemm_layout(args.h, stages, B, S);
   const int slot_w = lay.slot_w;
   uint8_t *s_w = smem;                                     // stages*B weight slots
   uint8_t *s_x = smem + lay.x_off;                         // stages*B activation slots
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * stages + 1);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * stages + 2);
+  float *red = reinterpret_cast<float *>(smem + lay.red_off);  // split-K exchange buffer
   volatile uint32_t *abort_flag = tmem_slot + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -82,6 +84,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = smem_u32(bars + stages);
   const uint32_t done_bar = smem_u32(bars + 2 * stages);
+  const uint32_t red_bar = smem_u32(bars + 2 * stages + 1);  // peers' partials arrived
 
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -89,6 +92,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(empty0 + 8 * s, kGemmIssuers);  // one commit per issuer
     }
     mbar_init(done_bar, kGemmIssuers);
+    mbar_init(red_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_map(&tmap_w);
@@ -102,6 +106,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // First phase of the cluster barrier: this CTA's exchange barrier is
+  // initialised. Peers wait on it only before their first push, long after.
+  if (S > 1) cluster_arrive();
 
   // Dependents may be scheduled as soon as every CTA of this grid is resident;
   // they order themselves after this grid with their own griddepcontrol.wait.
@@ -206,35 +213,79 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // Split-K across the S ranks of the cluster. Rank r owns tile rows
-    // [r * R, (r + 1) * R). Once every rank's MMAs are done (its ring is idle),
-    // each rank pushes its FP32 partial of every row into the owner's ring:
-    // red[q][t][row - r * R] for source rank q and token t. The owner then sums
-    // q = 0, 1, ..., S-1 in that order from its own shared memory.
-    const int S = args.splits;
+    // [r * R, (r + 1) * R). Every rank sends its FP32 partials of the rows it
+    // does not own to their owner (st.async into the owner's exchange buffer,
+    // red[q][row - r * R][t] for source rank q, counted on the owner's
+    // exchange barrier); the owner adds q = 0, 1, ..., S-1 in that order, its
+    // own partial taken from registers.
     const int R = (h + S - 1) / S;
     const uint32_t rank = cluster_ctarank();
-    float *red = reinterpret_cast<float *>(s_w);
-    const uint32_t red_base = smem_u32(red);
-    cluster_sync();  // all ranks past their MMAs
-    if (!aborted && tid < h) {
+    const int lo = static_cast<int>(rank) * R;
+    const int hi = min(h, lo + R);
+    const int ng = (m + 3) / 4;  // groups of 4 tokens sent
+    if (tid == 0)
+      mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>((S - 1) * max(0, hi - lo) * ng * 16));
+    cluster_wait();  // every peer's exchange barrier is initialised
+    if (tid < h) {
       const uint32_t owner = static_cast<uint32_t>(tid / R);
-      const int lr = tid - static_cast<int>(owner) * R;
-      const uint32_t dst = dsmem_map(red_base + static_cast<uint32_t>((rank * kTokTile * R + lr) * 4),
-                                     owner);
+      if (owner != rank) {
+        const int lr = tid - static_cast<int>(owner) * R;
+        const uint32_t dst =
+            dsmem_map(smem_u32(red + (static_cast<int>(rank) * R + lr) * kTokTile), owner);
+        const uint32_t rbar = dsmem_map(red_bar, owner);
 #pragma unroll
-      for (int t = 0; t < kTokTile; ++t)
-        if (t < m) dsmem_st_f32(dst + static_cast<uint32_t>(t * R * 4), acc[t]);
+        for (int g = 0; g < kTokTile / 4; ++g)
+          if (g < ng)
+            st_async_v4_f32(dst + 16 * g, acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3],
+                            rbar);
+      }
     }
-    cluster_sync();  // partials visible to their owners; no remote access after this
-    for (int o = tid; o < R * m; o += kGemmThreads) {
-      const int t = o / R;
-      const int lr = o - t * R;
-      const int row = static_cast<int>(rank) * R + lr;
-      if (row >= h) continue;
-      float v = red[t * R + lr];
-      for (int q = 1; q < S; ++q) v += red[(q * kTokTile + t) * R + lr];
-      if (!aborted && n0 + row < n) y[static_cast<size_t>(t) * n + n0 + row] = bf16_store_bits(v);
+    cluster_arrive();  // second phase: this CTA sends nothing more
+    if (tid >= lo && tid < hi) {
+      if (!mbar_wait_bounded(red_bar, 0, kWaitLimitNs)) {
+        atomicOr(&g_device_status, SK_DEVICE_WAIT_EPILOGUE);
+        *abort_flag = 1;
+      }
+      // All sums first, then the stores: a load issued after a global store
+      // that the compiler cannot prove disjoint waits behind it.
+      const int lr = tid - lo;
+      float v[kTokTile];
+#pragma unroll
+      for (int t = 0; t < kTokTile; ++t) v[t] = acc[t];
+      if (rank != 0) {
+        const float4 *r0 = reinterpret_cast<const float4 *>(red + lr * kTokTile);
+#pragma unroll
+        for (int g = 0; g < kTokTile / 4; ++g) {
+          const float4 p = r0[g];
+          v[4 * g] = p.x;
+          v[4 * g + 1] = p.y;
+          v[4 * g + 2] = p.z;
+          v[4 * g + 3] = p.w;
+        }
+      }
+      for (int q = 1; q < S; ++q) {
+        if (q == static_cast<int>(rank)) {
+#pragma unroll
+          for (int t = 0; t < kTokTile; ++t) v[t] += acc[t];
+        } else {
+          const float4 *rq = reinterpret_cast<const float4 *>(red + (q * R + lr) * kTokTile);
+#pragma unroll
+          for (int g = 0; g < kTokTile / 4; ++g) {
+            const float4 p = rq[g];
+            v[4 * g] += p.x;
+            v[4 * g + 1] += p.y;
+            v[4 * g + 2] += p.z;
+            v[4 * g + 3] += p.w;
+          }
+        }
+      }
+      if (!*abort_flag && n0 + tid < n) {
+#pragma unroll
+        for (int t = 0; t < kTokTile; ++t)
+          if (t < m) y[static_cast<size_t>(t) * n + n0 + tid] = bf16_store_bits(v[t]);
+      }
     }
+    cluster_wait();  // no peer writes into this CTA's shared memory any more
   }
 
   tc_fence_before_sync();
@@ -536,8 +587,8 @@ __global__ void convert_probe_kernel(int kind, const void *__restrict__ in, void
 namespace sk {
 
 // ---------------------------------------------------------------- host side
-size_t gemm_smem_bytes(int h, int stages, int bps) {
-  return 1024 + static_cast<size_t>(gemm_layout(h, stages, bps).total);
+size_t gemm_smem_bytes(int h, int stages, int bps, int splits) {
+  return 1024 + static_cast<size_t>(gemm_layout(h, stages, bps, splits).total);
 }
 
 namespace {
@@ -658,7 +709,7 @@ cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, ui
   a.splits = splits;
   a.rotate = rotate_k_order();
   const dim3 grid((n + h - 1) / h, splits, 1);
-  return launch_ex(gemm_kernel, grid, dim3(kGemmThreads), gemm_smem_bytes(h, stages, bps), stream, pdl,
+  return launch_ex(gemm_kernel, grid, dim3(kGemmThreads), gemm_smem_bytes(h, stages, bps, splits), stream, pdl,
                    dim3(1, splits, 1), tmap_w, tmap_x, a);
 }
 

@@ -262,6 +262,17 @@ __device__ __forceinline__ void dsmem_st_f32(uint32_t caddr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
 }
 
+// Four FP32 into a peer CTA's shared memory (16-byte aligned cluster address);
+// the 16 bytes count toward the transaction bytes of the peer's mbarrier.
+__device__ __forceinline__ void st_async_v4_f32(uint32_t caddr, float a, float b, float c, float d,
+                                                uint32_t cbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          caddr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(cbar)
+      : "memory");
+}
+
 // Split cluster barrier: arrive (release) now, wait (acquire) later.
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
