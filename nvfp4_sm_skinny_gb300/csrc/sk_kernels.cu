@@ -49,6 +49,30 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
   return true;
 }
 
+// Writes tile rows [r0, r1) of y (output features n0 + r0 ...; r1 - r0 and r0 a
+// multiple of 8): thread tid in [r0, r1) holds its row's 16 token values in v.
+// The values are staged as BF16 in shared memory, then each token's row
+// segment leaves in 16-byte stores (one per 8 features) instead of one 2-byte
+// store per token and feature. Called by all threads of the CTA.
+__device__ __forceinline__ void store_tile_rows(uint16_t *stage, const float (&v)[kTokTile], int r0,
+                                                int r1, uint16_t *y, int n, int n0, int m,
+                                                bool ok) {
+  const int tid = threadIdx.x, nr = r1 - r0;
+  if (tid >= r0 && tid < r1) {
+#pragma unroll
+    for (int t = 0; t < kTokTile; ++t) stage[t * nr + (tid - r0)] = bf16_store_bits(v[t]);
+  }
+  __syncthreads();
+  const int per_t = nr >> 3;
+  for (int c = tid; c < m * per_t; c += kGemmThreads) {
+    const int t = c / per_t, q = c - t * per_t;
+    const int row = n0 + r0 + 8 * q;
+    if (ok && row < n)
+      *reinterpret_cast<uint4 *>(y + static_cast<size_t>(t) * n + row) =
+          *reinterpret_cast<const uint4 *>(stage + t * nr + 8 * q);
+  }
+}
+
 // One CTA = h weight rows x one K slice of kb_per_split * 64 elements, moved
 // args.bps 64-column boxes per pipeline stage.
 // Warp 0 lane 0: TMA producer. Lane 0 of warps 1..kGemmIssuers: MMA issuers.
@@ -204,13 +228,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int m = args.m, n = args.n;
   uint16_t *y = args.y;
+  uint16_t *stage = reinterpret_cast<uint16_t *>(s_w);  // the ring is idle by now
   if (args.splits == 1) {
-    const int row = n0 + tid;
-    if (!aborted && tid < h && row < n) {
-#pragma unroll
-      for (int t = 0; t < kTokTile; ++t)
-        if (t < m) y[static_cast<size_t>(t) * n + row] = bf16_store_bits(acc[t]);
-    }
+    store_tile_rows(stage, acc, 0, h, y, n, n0, m, !aborted);
   } else {
     // Split-K across the S ranks of the cluster. Rank r owns tile rows
     // [r * R, (r + 1) * R). Every rank sends its FP32 partials of the rows it
@@ -241,6 +261,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
     cluster_arrive();  // second phase: this CTA sends nothing more
+    float v[kTokTile];
     if (tid >= lo && tid < hi) {
       if (!mbar_wait_bounded(red_bar, 0, kWaitLimitNs)) {
         atomicOr(&g_device_status, SK_DEVICE_WAIT_EPILOGUE);
@@ -249,7 +270,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // All sums first, then the stores: a load issued after a global store
       // that the compiler cannot prove disjoint waits behind it.
       const int lr = tid - lo;
-      float v[kTokTile];
 #pragma unroll
       for (int t = 0; t < kTokTile; ++t) v[t] = acc[t];
       if (rank != 0) {
@@ -279,11 +299,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      if (!*abort_flag && n0 + tid < n) {
+    }
+    __syncthreads();  // the exchange waits are over: *abort_flag is final
+    const bool ok = !*abort_flag;
+    if ((R & 7) == 0) {
+      store_tile_rows(stage, v, lo, hi > lo ? hi : lo, y, n, n0, m, ok);
+    } else if (ok && tid >= lo && tid < hi && n0 + tid < n) {
 #pragma unroll
-        for (int t = 0; t < kTokTile; ++t)
-          if (t < m) y[static_cast<size_t>(t) * n + n0 + tid] = bf16_store_bits(v[t]);
-      }
+      for (int t = 0; t < kTokTile; ++t)
+        if (t < m) y[static_cast<size_t>(t) * n + n0 + tid] = bf16_store_bits(v[t]);
     }
     cluster_wait();  // no peer writes into this CTA's shared memory any more
   }
