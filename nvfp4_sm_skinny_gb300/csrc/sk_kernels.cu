@@ -237,7 +237,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // does not own to their owner (st.async into the owner's exchange buffer,
     // red[q][row - r * R][t] for source rank q, counted on the owner's
     // exchange barrier); the owner adds q = 0, 1, ..., S-1 in that order, its
-    // own partial taken from registers.
+    // own partial taken from registers. A CTA leaves only after its exchange
+    // barrier has counted every byte its peers send it, so no peer writes into
+    // shared memory that is gone; one cluster barrier (before the first push)
+    // is enough.
     const int R = (h + S - 1) / S;
     const uint32_t rank = cluster_ctarank();
     const int lo = static_cast<int>(rank) * R;
@@ -260,7 +263,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             rbar);
       }
     }
-    cluster_arrive();  // second phase: this CTA sends nothing more
     float v[kTokTile];
     if (tid >= lo && tid < hi) {
       if (!mbar_wait_bounded(red_bar, 0, kWaitLimitNs)) {
@@ -309,7 +311,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int t = 0; t < kTokTile; ++t)
         if (t < m) y[static_cast<size_t>(t) * n + n0 + tid] = bf16_store_bits(v[t]);
     }
-    cluster_wait();  // no peer writes into this CTA's shared memory any more
   }
 
   tc_fence_before_sync();
