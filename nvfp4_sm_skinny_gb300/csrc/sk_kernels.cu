@@ -319,36 +319,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // ----------------------------------------------------------------------------
-// Block-wide FP32 sum in a fixed order: shuffle-down tree inside each warp,
-// then warp totals added in warp order by thread 0. `red` holds >= 33 floats.
-__device__ __forceinline__ float block_sum(float v, float *red) {
+// RMS factor of a row held by one CTA: the FP32 sum of v over the block in a
+// fixed order (shuffle-down tree inside each warp, then the warp totals in a
+// second shuffle-down tree in warp 0), and 1 / sqrt(sum / n + eps) computed
+// once with IEEE operations and handed to every thread. `red` holds >= 33
+// floats of shared memory.
+__device__ __forceinline__ float block_rms_inv(float v, float *red, float n, float eps) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_down_sync(0xffffffffu, v, off);
   if (lane == 0) red[warp] = v;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float s = red[0];
-    const int nw = (blockDim.x + 31) >> 5;
-    for (int i = 1; i < nw; ++i) s += red[i];
-    red[32] = s;
+  if (warp == 0) {
+    float t = lane < static_cast<int>(blockDim.x >> 5) ? red[lane] : 0.0f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_down_sync(0xffffffffu, t, off);
+    if (lane == 0) red[32] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, n), eps)));
   }
   __syncthreads();
   return red[32];
-}
-
-// Sum over the CTAs of a (csize, 1, 1) cluster of one value per CTA, in rank
-// order, so every CTA gets the same bits. `slot` is this CTA's shared word;
-// other ranks read it after the barrier, so the caller keeps the CTA alive
-// (a later cluster barrier) until they are done.
-__device__ __forceinline__ float cluster_total(float cta_part, float *slot, unsigned csize) {
-  if (csize == 1) return cta_part;
-  if (threadIdx.x == 0) *slot = cta_part;
-  cluster_sync();
-  const uint32_t a = smem_u32(slot);
-  float t = dsmem_ld_f32(dsmem_map(a, 0));
-  for (unsigned q = 1; q < csize; ++q) t += dsmem_ld_f32(dsmem_map(a, q));
-  return t;
 }
 
 __device__ __forceinline__ void unpack8(const uint4 &v, uint16_t (&o)[8]) {
@@ -394,20 +383,17 @@ __device__ __forceinline__ uint32_t nvfp4_block16(const uint16_t (&z)[16], float
 }
 
 // Pre-expert RMSNorm + NVFP4 (cutedsl/moe/pooler_gather, module docstring;
-// pooler_layer: weight applied after the norm). Token row i is spread over the
-// gridDim.x CTAs of one cluster; each thread owns one 16-column NVFP4 block.
+// pooler_layer: weight applied after the norm). One CTA per token row; each
+// thread owns one 16-column NVFP4 block.
 __global__ void __launch_bounds__(1024)
     rmsnorm_nvfp4_kernel(const uint16_t *__restrict__ y, const uint16_t *__restrict__ norm_w,
                          float eps, float gc, const float *__restrict__ gs_ptr,
                          uint8_t *__restrict__ a, uint8_t *__restrict__ a_sf,
                          uint16_t *__restrict__ z_out, int n) {
   __shared__ float red[33];
-  __shared__ float slot;
-  const unsigned csize = gridDim.x;
   const int row = blockIdx.y;
-  const int per_cta = (n >> 4) / static_cast<int>(csize);
-  const int blk = blockIdx.x * per_cta + threadIdx.x;
-  const bool active = static_cast<int>(threadIdx.x) < per_cta;
+  const int blk = threadIdx.x;
+  const bool active = blk < (n >> 4);
   griddep_launch_dependents();
 
   uint16_t w[16];
@@ -442,9 +428,7 @@ __global__ void __launch_bounds__(1024)
       ss = __fmaf_rn(f, f, ss);
     }
   }
-  ss = cluster_total(block_sum(ss, red), &slot, csize);
-  if (csize > 1) cluster_arrive();  // done reading the other ranks' slots
-  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(n)), eps)));
+  const float r = block_rms_inv(ss, red, static_cast<float>(n), eps);
 
   if (active) {
     uint16_t z[16];
@@ -471,7 +455,6 @@ __global__ void __launch_bounds__(1024)
       zp[1] = pack8(hi);
     }
   }
-  if (csize > 1) cluster_wait();  // keep `slot` alive until every rank has read it
 }
 
 // NVFP4 of a BF16 [m, n] tensor: one thread per 16-element block.
@@ -499,13 +482,17 @@ __global__ void __launch_bounds__(256)
   a_sf[base >> 4] = static_cast<uint8_t>(sf);
 }
 
-// Attention-boundary dual norm (cutedsl/oproj/batt, AttentionBoundary). Token
-// row i is spread over the gridDim.x CTAs of one cluster; each thread owns 8
-// consecutive columns.
+// Attention-boundary dual norm (cutedsl/oproj/batt, AttentionBoundary). One
+// CTA per token row; each thread owns 8 consecutive columns. The elementwise
+// steps use the packed FP32x2 operations (each lane an IEEE round-to-nearest
+// operation, the same as the scalar one) to halve the instruction count of a
+// row that one SM works through alone.
 constexpr int kDualThreads = 1024;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// the two BF16 of a 32-bit word as FP32 (low half first)
+__device__ __forceinline__ float2 bf16x2_f2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
 
 __global__ void __launch_bounds__(kDualThreads)
     dual_norm_kernel(const uint16_t *__restrict__ p, float *__restrict__ s,
@@ -514,12 +501,9 @@ __global__ void __launch_bounds__(kDualThreads)
                      uint16_t *__restrict__ out, float eps_post, float eps_pre, float gc_post,
                      float gc_pre, int h) {
   __shared__ float red1[33], red2[33];
-  __shared__ float slot1, slot2;
-  const unsigned csize = gridDim.x;
   const int row = blockIdx.y;
-  const int per_cta = (h >> 3) / static_cast<int>(csize);
-  const int ch = blockIdx.x * per_cta + threadIdx.x;
-  const bool active = static_cast<int>(threadIdx.x) < per_cta;
+  const int ch = threadIdx.x;
+  const bool active = ch < (h >> 3);
   griddep_launch_dependents();
 
   // Weights first (never written by a kernel), then wait for the producer of
@@ -533,58 +517,62 @@ __global__ void __launch_bounds__(kDualThreads)
   griddep_wait();
 
   const size_t rbase = static_cast<size_t>(row) * h;
-  float pv[8], sv[8];
+  float2 pv[4], sv[4];
   float ss1 = 0.0f;
   if (active) {
     const uint4 pw = reinterpret_cast<const uint4 *>(p + rbase)[ch];
     const float4 *sp = reinterpret_cast<const float4 *>(s + rbase) + 2 * ch;
     const float4 s0 = sp[0], s1 = sp[1];
-    pv[0] = bf16_lo(pw.x); pv[1] = bf16_hi(pw.x); pv[2] = bf16_lo(pw.y); pv[3] = bf16_hi(pw.y);
-    pv[4] = bf16_lo(pw.z); pv[5] = bf16_hi(pw.z); pv[6] = bf16_lo(pw.w); pv[7] = bf16_hi(pw.w);
-    sv[0] = s0.x; sv[1] = s0.y; sv[2] = s0.z; sv[3] = s0.w;
-    sv[4] = s1.x; sv[5] = s1.y; sv[6] = s1.z; sv[7] = s1.w;
+    pv[0] = bf16x2_f2(pw.x);
+    pv[1] = bf16x2_f2(pw.y);
+    pv[2] = bf16x2_f2(pw.z);
+    pv[3] = bf16x2_f2(pw.w);
+    sv[0] = make_float2(s0.x, s0.y);
+    sv[1] = make_float2(s0.z, s0.w);
+    sv[2] = make_float2(s1.x, s1.y);
+    sv[3] = make_float2(s1.z, s1.w);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) ss1 = __fmaf_rn(pv[j], pv[j], ss1);
+    for (int j = 0; j < 4; ++j) {
+      ss1 = __fmaf_rn(pv[j].x, pv[j].x, ss1);
+      ss1 = __fmaf_rn(pv[j].y, pv[j].y, ss1);
+    }
   }
-  ss1 = cluster_total(block_sum(ss1, red1), &slot1, csize);
-  const float r1 =
-      __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss1, static_cast<float>(h)), eps_post)));
+  const float r1 = block_rms_inv(ss1, red1, static_cast<float>(h), eps_post);
 
   float ss2 = 0.0f;
   if (active) {
     const uint32_t w1w[4] = {g1.x, g1.y, g1.z, g1.w};
     const uint32_t bw[4] = {gb.x, gb.y, gb.z, gb.w};
+    const float2 r1v = make_float2(r1, r1), av = make_float2(alpha, alpha);
+    const float2 gcv = make_float2(gc_post, gc_post);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t ww = w1w[j >> 1], bb = bw[j >> 1];
-      const float g = w1 ? __fadd_rn((j & 1) ? bf16_hi(ww) : bf16_lo(ww), gc_post) : 1.0f;
-      const float q = __fmul_rn(__fmul_rn(pv[j], r1), g);
-      const float bj = (j & 1) ? bf16_hi(bb) : bf16_lo(bb);
-      sv[j] = __fmaf_rn(bj, q, __fmul_rn(alpha, sv[j]));
-      ss2 = __fmaf_rn(sv[j], sv[j], ss2);
+    for (int j = 0; j < 4; ++j) {
+      const float2 g = w1 ? __fadd2_rn(bf16x2_f2(w1w[j]), gcv) : make_float2(1.0f, 1.0f);
+      const float2 q = __fmul2_rn(__fmul2_rn(pv[j], r1v), g);
+      sv[j] = __ffma2_rn(bf16x2_f2(bw[j]), q, __fmul2_rn(av, sv[j]));
+      ss2 = __fmaf_rn(sv[j].x, sv[j].x, ss2);
+      ss2 = __fmaf_rn(sv[j].y, sv[j].y, ss2);
     }
     float4 *sp = reinterpret_cast<float4 *>(s + rbase) + 2 * ch;
-    sp[0] = make_float4(sv[0], sv[1], sv[2], sv[3]);
-    sp[1] = make_float4(sv[4], sv[5], sv[6], sv[7]);
+    sp[0] = make_float4(sv[0].x, sv[0].y, sv[1].x, sv[1].y);
+    sp[1] = make_float4(sv[2].x, sv[2].y, sv[3].x, sv[3].y);
   }
-  ss2 = cluster_total(block_sum(ss2, red2), &slot2, csize);
-  if (csize > 1) cluster_arrive();  // done reading the other ranks' slots
-  const float r2 =
-      __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss2, static_cast<float>(h)), eps_pre)));
+  const float r2 = block_rms_inv(ss2, red2, static_cast<float>(h), eps_pre);
 
   if (active) {
     const uint32_t w2w[4] = {g2.x, g2.y, g2.z, g2.w};
+    const float2 r2v = make_float2(r2, r2), gcv = make_float2(gc_pre, gc_pre);
     uint16_t o[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t ww = w2w[j >> 1];
-      const float g = __fadd_rn((j & 1) ? bf16_hi(ww) : bf16_lo(ww), gc_pre);
-      o[j] = bf16_store_bits(__fmul_rn(__fmul_rn(sv[j], r2), g));
+    for (int j = 0; j < 4; ++j) {
+      const float2 v = __fmul2_rn(__fmul2_rn(sv[j], r2v), __fadd2_rn(bf16x2_f2(w2w[j]), gcv));
+      o[2 * j] = bf16_store_bits(v.x);
+      o[2 * j + 1] = bf16_store_bits(v.y);
     }
     reinterpret_cast<uint4 *>(out + rbase)[ch] = pack8(o);
   }
-  if (csize > 1) cluster_wait();  // keep the slots alive until every rank has read them
 }
+
 
 // Format-conversion probe over n inputs (see sk_convert_probe).
 __global__ void convert_probe_kernel(int kind, const void *__restrict__ in, void *__restrict__ out,
@@ -738,27 +726,12 @@ cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, ui
                    dim3(1, splits, 1), tmap_w, tmap_x, a);
 }
 
-// CTAs per token row of the norm kernels (a cluster): 1 by default (measured
-// fastest: the kernels are latency-bound and a cluster barrier costs more than
-// it saves); SK_TAIL_CLUSTER (1, 2, 4 or 8) overrides.
-static int tail_cluster_max() {
-  static const int c = [] {
-    const char *v = std::getenv("SK_TAIL_CLUSTER");
-    const int x = v ? std::atoi(v) : 1;
-    return (x == 1 || x == 2 || x == 4 || x == 8) ? x : 1;
-  }();
-  return c;
-}
-
 cudaError_t launch_rmsnorm_nvfp4(const uint16_t *y, const uint16_t *norm_w, float eps, float gc,
                                  const float *gs, uint8_t *a, uint8_t *a_sf, uint16_t *z_out,
                                  int m, int n, cudaStream_t stream, bool pdl) {
-  // a cluster of up to 8 CTAs per token row, at least one warp of blocks each
-  const int nblk = n / 16;
-  int c = tail_cluster_max();
-  while (c > 1 && (nblk % c || nblk / c < 32)) c /= 2;
-  const int threads = (nblk / c + 31) / 32 * 32;
-  return launch_ex(rmsnorm_nvfp4_kernel, dim3(c, m), dim3(threads), 0, stream, pdl, dim3(c, 1, 1),
+  // one CTA per token row, one thread per 16-column block (n <= 16384)
+  const int threads = (n / 16 + 31) / 32 * 32;
+  return launch_ex(rmsnorm_nvfp4_kernel, dim3(1, m), dim3(threads), 0, stream, pdl, dim3(1, 1, 1),
                    y, norm_w, eps, gc, gs, a, a_sf, z_out, n);
 }
 
@@ -774,13 +747,10 @@ cudaError_t launch_dual_norm(const uint16_t *p, float *s, const uint16_t *w1, fl
                              const uint16_t *beta, const uint16_t *w2, uint16_t *out,
                              float eps_post, float eps_pre, float gc_post, float gc_pre, int m,
                              int h, cudaStream_t stream, bool pdl) {
-  // a cluster of up to 8 CTAs per token row, at least two warps of chunks each
-  // (h <= 8 * kDualThreads is checked by the caller)
-  const int nchunk = h / 8;
-  int c = tail_cluster_max();
-  while (c > 1 && (nchunk % c || nchunk / c < 64)) c /= 2;
-  const int threads = (nchunk / c + 31) / 32 * 32;
-  return launch_ex(dual_norm_kernel, dim3(c, m), dim3(threads), 0, stream, pdl, dim3(c, 1, 1), p, s,
+  // one CTA per token row, 8 columns per thread (h <= 8 * kDualThreads is
+  // checked by the caller)
+  const int threads = (h / 8 + 31) / 32 * 32;
+  return launch_ex(dual_norm_kernel, dim3(1, m), dim3(threads), 0, stream, pdl, dim3(1, 1, 1), p, s,
                    w1, alpha, beta, w2, out, eps_post, eps_pre, gc_post, gc_pre, h);
 }
 
