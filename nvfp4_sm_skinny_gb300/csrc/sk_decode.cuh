@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kBlockK / 16; ++kk)
               tc_mma_bf16(tmem + static_cast<uint32_t>(acc_index(q, kk) * kTokTile), adesc + 2 * kk,
-                          bdesc + 2 * kk, kIdesc, started);
+                          bdesc + 2 * kk, kIdesc, started || kk > 0);
             started = true;
           }
           tc_commit(empty0 + 8 * s);

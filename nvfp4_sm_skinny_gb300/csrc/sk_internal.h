@@ -36,20 +36,22 @@ constexpr int kMaxStages = 16;
 // instruction whatever its M and N (measured on GB300: ~75 ns), which at
 // 128 x 16 x 16 caps one issuer at ~55 GB/s of weight; the rate grows with the
 // number of issuing warps per SM. So a CTA issues from several warps: box j of
-// a stage goes to issuer j mod NI, and issuer q's k-step kk accumulates into
-// its own TMEM accumulator q * 4 + kk (16 FP32 columns), first written by the
-// issuer's first box of the slice. The epilogue adds the used accumulators in
-// index order, so the sum order is fixed.
-constexpr int kGemmIssuers = 2;
-constexpr int kNumAcc = kGemmIssuers * (kBlockK / 16);  // 8
-constexpr int kTmemCols = kNumAcc * kTokTile;           // 128
-__host__ __device__ constexpr int acc_index(int q, int kk) { return q * (kBlockK / 16) + kk; }
+// a stage goes to issuer j mod NI, and issuer q accumulates into its own TMEM
+// accumulator (16 FP32 columns), first written by the issuer's first box of
+// the slice (the issue cost, not the chained accumulation, sets the rate).
+// The epilogue adds the used accumulators in index order, so the sum order is
+// fixed.
+constexpr int kGemmIssuers = 4;
+constexpr int kNumAcc = kGemmIssuers;           // one per issuer
+constexpr int kTmemCols = 64;                   // kNumAcc * kTokTile, a power of two >= 32
+static_assert(kNumAcc * kTokTile <= kTmemCols, "accumulators exceed the TMEM allocation");
+__host__ __device__ constexpr int acc_index(int q, int /*kk*/) { return q; }
 // Accumulators written by a K slice of nkb boxes moved bps per stage by ni
 // issuers: those of the issuers that own a box of the first stage.
 __host__ __device__ inline int acc_used(int nkb, int bps, int ni) {
   int b = nkb < bps ? nkb : bps;
   if (b > ni) b = ni;
-  return b * (kBlockK / 16);
+  return b;
 }
 // K order. Every CTA of a row of tiles reads the same activation boxes; walked
 // in lockstep from k = 0, all of them would ask the same few L2 lines for the
@@ -148,8 +150,8 @@ cudaError_t read_device_status(uint32_t *out, bool clear);
 // quadrant.
 constexpr int kDecIssuers = 4;
 constexpr int kDecThreads = 32 * (1 + kDecIssuers + 4);
-constexpr int kDecNumAcc = kDecIssuers * (kBlockK / 16);  // 16
-constexpr int kDecTmemCols = kDecNumAcc * kTokTile;       // 256
+constexpr int kDecNumAcc = kDecIssuers;              // one accumulator per issuer
+constexpr int kDecTmemCols = kDecNumAcc * kTokTile;  // 64
 constexpr int kDecPhases = 3;  // 0: o_proj, 1: pooler, 2: unpooler
 
 struct DecodeMaps {

@@ -24,7 +24,10 @@ __device__ uint32_t g_device_status;
 
 constexpr uint32_t kIdesc = idesc_bf16_f32(kMmaM, kTokTile);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s of wall time per wait
-constexpr int kGemmThreads = 128;                  // 4 warps = the 128 TMEM lanes
+// Warps 0-3 hold the 128 TMEM lanes in the epilogue (thread t = lane t);
+// warp 4 only issues MMAs.
+constexpr int kGemmThreads = 32 * (1 + kGemmIssuers);
+static_assert(kGemmThreads >= 128, "the epilogue needs four warps");
 
 struct GemmArgs {
   uint16_t *y;       // [m, n] BF16 bits
@@ -76,8 +79,8 @@ __device__ __forceinline__ void store_tile_rows(uint16_t *stage, const float (&v
 // One CTA = h weight rows x one K slice of kb_per_split * 64 elements, moved
 // args.bps 64-column boxes per pipeline stage.
 // Warp 0 lane 0: TMA producer. Lane 0 of warps 1..kGemmIssuers: MMA issuers.
-// Warp 2 owns the TMEM allocation. All four warps run the epilogue (one TMEM
-// lane per thread).
+// Warp 2 owns the TMEM allocation. Warps 0-3 run the epilogue (one TMEM lane
+// per thread).
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                 GemmArgs args) {
@@ -194,7 +197,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int kk = 0; kk < kBlockK / 16; ++kk) {
           // K advances 16 elements = 32 bytes inside the 128-byte swizzle row.
           tc_mma_bf16(tmem + static_cast<uint32_t>(acc_index(q, kk) * kTokTile), adesc + 2 * kk,
-                      bdesc + 2 * kk, kIdesc, started);
+                      bdesc + 2 * kk, kIdesc, started || kk > 0);
         }
         started = true;
       }
@@ -220,8 +223,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after_sync();
 
   float acc[kTokTile];
-  tmem_sum_accumulators<kNumAcc>(tmem + (static_cast<uint32_t>(warp * 32) << 16),
-                                 acc_used(nkb, B, kGemmIssuers), acc);
+  if (warp < 4)
+    tmem_sum_accumulators<kNumAcc>(tmem + (static_cast<uint32_t>(warp * 32) << 16),
+                                   acc_used(nkb, B, kGemmIssuers), acc);
 
   // Outputs may still be read by the previous kernel in the stream.
   griddep_wait();
