@@ -38,6 +38,7 @@ struct GemmArgs {
   int bps;           // boxes per stage
   int splits;
   int rotate;        // 1: stagger the K order across row tiles
+  int l2_ahead;      // weight stages started towards L2 before the dependency wait
 };
 
 // Bounded wait that also gives up as soon as another role raised `abort`.
@@ -157,6 +158,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tma_load_3d(smem_u32(s_w + i * B * slot_w), &tmap_w, full0 + 8 * i, 0, n0,
                   kb0 + rotated_stage(i, rot, nst) * B, pol_w);
     }
+    // and the next stages towards L2, while the previous kernel finishes
+    for (int i = npre; i < nst && i < npre + args.l2_ahead; ++i)
+      tma_prefetch_l2_3d(&tmap_w, 0, n0, kb0 + rotated_stage(i, rot, nst) * B);
     griddep_wait();
     for (int i = 0; i < npre; ++i)
       tma_load_3d(smem_u32(s_x + i * B * kSlotXBytes), &tmap_x, full0 + 8 * i, 0, 0,
@@ -725,6 +729,17 @@ cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, ui
   a.bps = bps;
   a.splits = splits;
   a.rotate = rotate_k_order();
+  // Weight stages started towards L2 before the dependency wait, beyond the
+  // ring: about 256 KiB per CTA (measured best on the decode chain: the
+  // previous kernel's tail and the norm between two GEMMs leave HBM idle;
+  // much more slows that norm's own memory accesses). SK_L2_AHEAD overrides.
+  {
+    const char *v = std::getenv("SK_L2_AHEAD");
+    const int stage_w = bps * h * 128;
+    a.l2_ahead = v ? std::atoi(v) : (256 * 1024 + stage_w - 1) / stage_w;
+    if (a.l2_ahead < 0) a.l2_ahead = 0;
+    if (a.l2_ahead > 64) a.l2_ahead = 64;
+  }
   const dim3 grid((n + h - 1) / h, splits, 1);
   return launch_ex(gemm_kernel, grid, dim3(kGemmThreads), gemm_smem_bytes(h, stages, bps, splits), stream, pdl,
                    dim3(1, splits, 1), tmap_w, tmap_x, a);
