@@ -488,7 +488,6 @@ sk_status sk_decode_layer(const void *h_in, const void *w_o, const void *w_p, co
          sk::decode_smem_bytes(slot_w, args.stages + 1, args.bps) <= cap)
     ++args.stages;
   const size_t smem = sk::decode_smem_bytes(slot_w, args.stages, args.bps);
-  args.rotate = sk::rotate_k_order();
   if (sk::decode_blocks_per_sm(smem) < 1)
     return fail(SK_ERR_UNSUPPORTED, "the fused layer kernel cannot be resident with %zu bytes", smem);
   args.post_w = static_cast<const uint16_t *>(post_w);

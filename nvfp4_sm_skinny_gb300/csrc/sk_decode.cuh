@@ -187,16 +187,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const uint32_t done0 = smem_u32(bars + 2 * S);
 
   // stage sequence of this CTA: the phases it has a tile in, in order
-  int nst[kDecPhases], st0[kDecPhases], rot[kDecPhases], total = 0;
+  int nst[kDecPhases], st0[kDecPhases], total = 0;
 #pragma unroll
   for (int p = 0; p < kDecPhases; ++p) {
     nst[p] = c < args.tiles[p] ? (args.nkb[p] + B - 1) / B : 0;
     st0[p] = total;
     total += nst[p];
-    rot[p] = args.rotate ? stage_rotation(c, args.tiles[p], nst[p]) : 0;
   }
   // first 64-wide K block of stage ls of phase p
-  auto kb_of = [&](int ls, int p) { return rotated_stage(ls, rot[p], nst[p]) * B; };
+  auto kb_of = [&](int ls, int /*p*/) { return ls * B; };
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {

@@ -53,19 +53,6 @@ __host__ __device__ inline int acc_used(int nkb, int bps, int ni) {
   if (b > ni) b = ni;
   return b;
 }
-// K order. Every CTA of a row of tiles reads the same activation boxes; walked
-// in lockstep from k = 0, all of them would ask the same few L2 lines for the
-// same box at once and queue on them. So tile r of G walks its nst stages
-// starting at stage rot = floor(r * nst / G) and wraps around: at any moment
-// the CTAs spread their activation reads over the whole of x. The order is
-// fixed by the launch shape, so results stay bitwise reproducible.
-__host__ __device__ inline int stage_rotation(int r, int G, int nst) {
-  return nst > 1 ? static_cast<int>((static_cast<long long>(r) * nst) / G) % nst : 0;
-}
-__host__ __device__ inline int rotated_stage(int i, int rot, int nst) {
-  const int v = i + rot;
-  return v >= nst ? v - nst : v;
-}
 // Shared memory per CTA when two CTAs share an SM.
 constexpr size_t kTwoPerSmSmem = 110 * 1024;
 // Shared memory per CTA when one CTA owns an SM.
@@ -124,9 +111,6 @@ cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, ui
                         int n, int k, int splits, int h, int stages, int bps, cudaStream_t stream,
                         bool pdl);
 
-// 1 unless the environment sets SK_ROTATE=0: stagger the K order of row tiles.
-int rotate_k_order();
-
 cudaError_t launch_rmsnorm_nvfp4(const uint16_t *y, const uint16_t *norm_w, float eps, float gc,
                                  const float *gs, uint8_t *a, uint8_t *a_sf, uint16_t *z_out,
                                  int m, int n, cudaStream_t stream, bool pdl);
@@ -165,7 +149,6 @@ struct DecodeArgs {
   int tiles[kDecPhases];  // CTA c owns tile c of phase p when c < tiles[p]
   int nkb[kDecPhases];    // 64-wide K blocks per phase
   int stages, bps;        // pipeline stages, boxes per stage
-  int rotate;             // 1: stagger the K order across tiles
   int slot_w;             // bytes per weight slot
   const uint16_t *post_w, *beta, *pre_w, *norm_w;
   float alpha, eps_post, eps_pre, gc_post, gc_pre, eps_pool, gc_pool;

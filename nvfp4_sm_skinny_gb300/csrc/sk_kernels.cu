@@ -37,7 +37,6 @@ struct GemmArgs {
   int stages;
   int bps;           // boxes per stage
   int splits;
-  int rotate;        // 1: stagger the K order across row tiles
   int l2_ahead;      // weight stages started towards L2 before the dependency wait
 };
 
@@ -106,7 +105,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int nkb = args.kb_per_split;
   const int kb0 = blockIdx.y * nkb;
   const int nst = (nkb + B - 1) / B;                     // pipeline stages of work
-  const int rot = args.rotate ? stage_rotation(blockIdx.x, gridDim.x, nst) : 0;
   const uint32_t stage_tx = static_cast<uint32_t>(B * (h * 128 + kSlotXBytes));
 
   const uint32_t full0 = smem_u32(bars);
@@ -155,16 +153,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // before waiting for the previous kernel in the stream.
     for (int i = 0; i < npre; ++i) {
       mbar_arrive_expect_tx(full0 + 8 * i, stage_tx);
-      tma_load_3d(smem_u32(s_w + i * B * slot_w), &tmap_w, full0 + 8 * i, 0, n0,
-                  kb0 + rotated_stage(i, rot, nst) * B, pol_w);
+      tma_load_3d(smem_u32(s_w + i * B * slot_w), &tmap_w, full0 + 8 * i, 0, n0, kb0 + i * B,
+                  pol_w);
     }
     // and the next stages towards L2, while the previous kernel finishes
     for (int i = npre; i < nst && i < npre + args.l2_ahead; ++i)
-      tma_prefetch_l2_3d(&tmap_w, 0, n0, kb0 + rotated_stage(i, rot, nst) * B);
+      tma_prefetch_l2_3d(&tmap_w, 0, n0, kb0 + i * B);
     griddep_wait();
     for (int i = 0; i < npre; ++i)
-      tma_load_3d(smem_u32(s_x + i * B * kSlotXBytes), &tmap_x, full0 + 8 * i, 0, 0,
-                  kb0 + rotated_stage(i, rot, nst) * B, pol_x);
+      tma_load_3d(smem_u32(s_x + i * B * kSlotXBytes), &tmap_x, full0 + 8 * i, 0, 0, kb0 + i * B,
+                  pol_x);
     issued = npre;
     for (int i = npre; i < nst; ++i) {
       const int s = i % stages;
@@ -174,7 +172,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         *abort_flag = 1;
         break;
       }
-      const int kb = kb0 + rotated_stage(i, rot, nst) * B;
+      const int kb = kb0 + i * B;
       mbar_arrive_expect_tx(full0 + 8 * s, stage_tx);
       tma_load_3d(smem_u32(s_w + s * B * slot_w), &tmap_w, full0 + 8 * s, 0, n0, kb, pol_w);
       tma_load_3d(smem_u32(s_x + s * B * kSlotXBytes), &tmap_x, full0 + 8 * s, 0, 0, kb, pol_x);
@@ -193,7 +191,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const int nb = min(B, nkb - rotated_stage(i, rot, nst) * B);
+      const int nb = min(B, nkb - i * B);
       for (int j = q; j < nb; j += kGemmIssuers) {
         const uint64_t adesc = smem_desc_k128(smem_u32(s_w + (s * B + j) * slot_w));
         const uint64_t bdesc = smem_desc_k128(smem_u32(s_x + (s * B + j) * kSlotXBytes));
@@ -709,12 +707,6 @@ int gemm_max_clusters(int device, int splits, int ctas_per_sm) {
   return cache[device][idx][per];
 }
 
-// Staggered K order across row tiles: on unless SK_ROTATE=0 (for comparison).
-int rotate_k_order() {
-  const char *v = std::getenv("SK_ROTATE");
-  return (v && v[0] == '0') ? 0 : 1;
-}
-
 cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, uint16_t *y, int m,
                         int n, int k, int splits, int h, int stages, int bps,
                         cudaStream_t stream, bool pdl) {
@@ -728,7 +720,6 @@ cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, ui
   a.stages = stages;
   a.bps = bps;
   a.splits = splits;
-  a.rotate = rotate_k_order();
   // Weight stages started towards L2 before the dependency wait, beyond the
   // ring: about 256 KiB per CTA (measured best on the decode chain: the
   // previous kernel's tail and the norm between two GEMMs leave HBM idle;
