@@ -442,6 +442,110 @@ def run_gpu(args, world, rank, local):
     return 0
 
 
+# ---------------------------------------------------------------- sweep ----
+def run_sweep(args, local):
+    """Per-call timings of the single-call workloads (GEMM at M = 1..16 and
+    every split count, pooler + RMSNorm + NVFP4, o_proj + dual norm): each
+    point is a CUDA graph of one call per weight copy (48 copies drawn on the
+    device, more bytes than L2), replayed after warm-up; µs/call, algorithmic
+    GB/s and % of the HBM peak. One JSON line per point, then a markdown
+    table."""
+    import torch
+
+    from __graft_entry__ import build
+    build()
+    import nvfp4_sm_skinny_gb300 as sk
+    from nvfp4_sm_skinny_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peak, peak_src = hbm_peak()
+    stream = torch.cuda.Stream(dev)
+    copies = 48
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    rows = []
+
+    def per_call(calls, min_calls=200):
+        with torch.cuda.stream(stream):
+            for c in calls:
+                c()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for c in calls:
+                c()
+        for _ in range(3):
+            with torch.cuda.stream(stream):
+                g.replay()
+        reps = max(3, -(-min_calls // len(calls)))
+        best = min(time_graph(g, reps, stream) for _ in range(3))
+        return best / (reps * len(calls))
+
+    def record(workload, m, n, k, splits, sec, nbytes):
+        gbs = nbytes / sec / 1e9
+        r = dict(workload=workload, m=m, n=n, k=k, splits=splits, us_per_call=round(sec * 1e6, 3),
+                 gbs=round(gbs, 1), pct_of_peak=round(100 * gbs / peak, 1), bytes=nbytes)
+        rows.append(r)
+        print(json.dumps(r), flush=True)
+
+    # GEMM (the unpooler shard and the sweep)
+    for n, k in ((1024, 4096), (8192, 4096)):
+        ws = [synth.gemm_weight(n, k, i, device=dev) for i in range(copies)]
+        for m in (1, 2, 4, 8, 16):
+            x = synth.gemm_x(m, k).to(dev)
+            y = torch.empty(m, n, **bf)
+            for S in (0, 1, 2, 4, 8):
+                if sk.gemm_supported(m, n, k, S) is not None:
+                    continue
+                sec = per_call([lambda w=w, S=S: sk.gemm_bf16(x, w, out=y, splits=S, stream=stream)
+                                for w in ws])
+                record("gemm", m, n, k, S if S else f"auto({sk.gemm_splits(m, n, k)})", sec,
+                       2 * n * k + 2 * m * k + 2 * m * n)
+        del ws
+        torch.cuda.empty_cache()
+    # pooler GEMM + pre-expert RMSNorm + NVFP4
+    H, P = synth.HIDDEN, synth.POOLED
+    ws = [synth.normal_bf16((P, H), 0.02, 200 + i, device=dev) for i in range(copies)]
+    nw = synth.normal_bf16((P,), 0.1, 300, device=dev)
+    gs = torch.tensor([300.0], dtype=torch.float32, device=dev)
+    for b in (1, 8, 16):
+        x = synth.normal_bf16((b, H), 1.0, 0, device=dev)
+        a = torch.empty(b, P // 2, dtype=torch.uint8, device=dev)
+        a_sf = torch.empty(b, P // 16, dtype=torch.uint8, device=dev)
+        wsp = torch.empty(sk.gemm_rmsnorm_nvfp4_workspace(b, P), dtype=torch.uint8, device=dev)
+        sec = per_call([lambda w=w: sk.gemm_rmsnorm_nvfp4(x, w, nw, synth.EPS, synth.GAIN_CENTER, gs,
+                                                          a=a, a_sf=a_sf, workspace=wsp, stream=stream)
+                        for w in ws])
+        record("pooler+rmsnorm+nvfp4", b, P, H, f"auto({sk.gemm_splits(b, P, H)})", sec,
+               2 * P * H + 2 * b * H + 2 * P + 4 + b * P // 2 + b * P // 16)
+    del ws
+    torch.cuda.empty_cache()
+    # o_proj GEMM + dual norm (the residual stream drifts from call to call)
+    K = synth.OPROJ_K
+    ws = [synth.normal_bf16((H, K), 0.02, 400 + i, device=dev) for i in range(copies)]
+    post_w = synth.normal_bf16((H,), 0.1, 500, mean=1.0, device=dev)
+    pre_w = synth.normal_bf16((H,), 0.1, 501, mean=1.0, device=dev)
+    beta = synth.uniform_bf16((H,), 0.5, 1.5, 502, device=dev)
+    for b in (1, 4, 16):
+        x = synth.normal_bf16((b, K), 1.0, 0, device=dev)
+        s_res = synth.normal_f32((b, H), 503, device=dev)
+        out = torch.empty(b, H, **bf)
+        wsp = torch.empty(sk.gemm_dual_norm_workspace(b, H), dtype=torch.uint8, device=dev)
+        sec = per_call([lambda w=w: sk.gemm_dual_norm(x, w, s_res, post_w, 1.0, beta, pre_w, out=out,
+                                                      eps_post=synth.EPS, eps_pre=synth.EPS,
+                                                      workspace=wsp, stream=stream)
+                        for w in ws])
+        record("oproj+dual_norm", b, H, K, f"auto({sk.gemm_splits(b, H, K)})", sec,
+               2 * H * K + 2 * b * K + 3 * 2 * H + 2 * 4 * b * H + 2 * b * H)
+    print(f"\n| workload | M | N | K | splits | µs/call | GB/s | % of {peak_src} peak ({peak:.0f} GB/s) |")
+    print("|---|---|---|---|---|---|---|---|")
+    for r in rows:
+        print(f"| {r['workload']} | {r['m']} | {r['n']} | {r['k']} | {r['splits']} | "
+              f"{r['us_per_call']:.2f} | {r['gbs']:.0f} | {r['pct_of_peak']:.1f} |")
+    print(f"\ndevice status {sk.device_status()}")
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -452,10 +556,14 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="chain depth (48 is the benchmark; fewer only for small profiling runs)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="per-call timings of the single-call workloads instead of the chain")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()
+    if args.sweep:
+        return run_sweep(args, local)
     if args.impl == "reference":
         return run_reference(args, world, rank)
     return run_gpu(args, world, rank, local)

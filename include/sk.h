@@ -118,6 +118,31 @@ sk_status sk_rmsnorm_nvfp4(const void *y, const void *norm_w, float eps, float g
                            const float *global_scale, uint8_t *a, uint8_t *a_sf, void *z_out,
                            int m, int n, void *stream);
 
+/*
+ * sk_rmsnorm_bf16 -- pre-expert RMSNorm of a BF16 edge layer: the rows the
+ * experts take in BF16 instead of NVFP4 (cutedsl/moe/pooler_gather, module
+ * docstring, "BF16 edge layers" / ExpertsInputBf16, and the ExpertNorm launch
+ * in Pooler's edge-layer path). Same norm as sk_rmsnorm_nvfp4's z:
+ *   z = bf16(y * rsqrt(mean(y^2) + eps) * (norm_w + gain_center)), -0 -> +0.
+ *   y BF16 [m, n], norm_w BF16 [n], z BF16 [m, n]; 1 <= m <= 16, n a multiple
+ *   of 16 in [16, 16384]; all pointers 16-byte aligned.
+ */
+sk_status sk_rmsnorm_bf16(const void *y, const void *norm_w, float eps, float gain_center, void *z,
+                          int m, int n, void *stream);
+
+/*
+ * sk_gemm_rmsnorm_bf16 -- the pooler for a BF16 edge layer: y = x @ w^T (as
+ * sk_gemm_bf16, into the workspace), then sk_rmsnorm_bf16 of y into z
+ * (cutedsl/moe/pooler_gather, Pooler.run for a layer without a global scale:
+ * it returns the normalised BF16 rows). Workspace: at least
+ * sk_gemm_rmsnorm_nvfp4_workspace(m, n) bytes, 256-byte aligned; it holds y
+ * on return. Constraints are those of sk_gemm_bf16 and sk_rmsnorm_bf16.
+ */
+sk_status sk_gemm_rmsnorm_bf16(const void *x, const void *w, const void *norm_w, float eps,
+                               float gain_center, void *z, void *workspace,
+                               size_t workspace_bytes, int m, int n, int k, int splits,
+                               void *stream);
+
 /* Size in bytes of the workspace sk_gemm_rmsnorm_nvfp4 needs for (m, n): the
    BF16 GEMM output that the norm reads back (m * n * 2, rounded up to 256). */
 size_t sk_gemm_rmsnorm_nvfp4_workspace(int m, int n);

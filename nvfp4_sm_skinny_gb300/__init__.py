@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
             "sk_gemm_rmsnorm_nvfp4_workspace": ([i, i], sz),
             "sk_gemm_rmsnorm_nvfp4": ([vp, vp, vp, f, f, vp, vp, vp, vp, vp, sz, i, i, i, i, vp], i),
             "sk_nvfp4_quantize": ([vp, vp, vp, vp, i, i, vp], i),
+            "sk_rmsnorm_bf16": ([vp, vp, f, f, vp, i, i, vp], i),
+            "sk_gemm_rmsnorm_bf16": ([vp, vp, vp, f, f, vp, vp, sz, i, i, i, i, vp], i),
             "sk_dual_norm_residual": ([vp, vp, vp, f, vp, vp, vp, f, f, f, f, i, i, vp], i),
             "sk_gemm_dual_norm_workspace": ([i, i], sz),
             "sk_gemm_dual_norm": ([vp, vp, vp, vp, f, vp, vp, vp, f, f, f, f, vp, sz, i, i, i, i, vp], i),
@@ -178,6 +180,40 @@ def rmsnorm_nvfp4(y, norm_w, eps: float, gain_center: float, global_scale, a=Non
     _check(lib().sk_rmsnorm_nvfp4(_ptr(y), _ptr(norm_w), eps, gain_center, _ptr(global_scale),
                                   _ptr(a), _ptr(a_sf), _ptr(z_out), m, n, _stream(stream)))
     return a, a_sf, z_out
+
+
+def rmsnorm_bf16(y, norm_w, eps: float, gain_center: float, out=None, stream=None):
+    """z BF16 [m, n]: pre-expert RMSNorm of a BF16 edge layer (no NVFP4)."""
+    m, n = y.shape
+    _need(y, torch.bfloat16, (m, n), "y")
+    _need(norm_w, torch.bfloat16, (n,), "norm_w")
+    if out is None:
+        out = torch.empty(m, n, dtype=torch.bfloat16, device=y.device)
+    _need(out, torch.bfloat16, (m, n), "out")
+    _check(lib().sk_rmsnorm_bf16(_ptr(y), _ptr(norm_w), eps, gain_center, _ptr(out), m, n,
+                                 _stream(stream)))
+    return out
+
+
+def gemm_rmsnorm_bf16(x, w, norm_w, eps: float, gain_center: float, out=None, workspace=None,
+                      splits: int = 0, stream=None):
+    """(z, workspace): the pooler GEMM then the pre-expert RMSNorm of a BF16
+    edge layer. The workspace (uint8) holds the BF16 GEMM output on return."""
+    m, k = x.shape
+    n = w.shape[0]
+    _need(x, torch.bfloat16, (m, k), "x")
+    _need(w, torch.bfloat16, (n, k), "w")
+    _need(norm_w, torch.bfloat16, (n,), "norm_w")
+    if out is None:
+        out = torch.empty(m, n, dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, (m, n), "out")
+    if workspace is None:
+        workspace = torch.empty(gemm_rmsnorm_nvfp4_workspace(m, n), dtype=torch.uint8,
+                                device=x.device)
+    _check(lib().sk_gemm_rmsnorm_bf16(
+        _ptr(x), _ptr(w), _ptr(norm_w), eps, gain_center, _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), m, n, k, splits, _stream(stream)))
+    return out, workspace
 
 
 def gemm_rmsnorm_nvfp4_workspace(m: int, n: int) -> int:

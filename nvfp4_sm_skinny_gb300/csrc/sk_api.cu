@@ -345,6 +345,44 @@ sk_status sk_gemm_rmsnorm_nvfp4(const void *x, const void *w, const void *norm_w
       "rmsnorm_nvfp4");
 }
 
+sk_status sk_rmsnorm_bf16(const void *y, const void *norm_w, float eps, float gain_center, void *z,
+                          int m, int n, void *stream) {
+  sk_status st;
+  if ((st = check_norm_quant(m, n)) != SK_OK) return st;
+  if ((st = check_ptrs16("sk_rmsnorm_bf16(y, norm_w, z)", {y, norm_w, z})) != SK_OK) return st;
+  sk::DeviceInfo info;
+  if ((st = current_device(&info)) != SK_OK) return st;
+  return launch_status(
+      sk::launch_rmsnorm_nvfp4(static_cast<const uint16_t *>(y), static_cast<const uint16_t *>(norm_w),
+                               eps, gain_center, nullptr, nullptr, nullptr,
+                               static_cast<uint16_t *>(z), m, n, as_stream(stream), pdl_enabled()),
+      "rmsnorm_bf16");
+}
+
+sk_status sk_gemm_rmsnorm_bf16(const void *x, const void *w, const void *norm_w, float eps,
+                               float gain_center, void *z, void *workspace,
+                               size_t workspace_bytes, int m, int n, int k, int splits,
+                               void *stream) {
+  sk_status st;
+  if ((st = check_gemm_shape(m, n, k, splits)) != SK_OK) return st;
+  if ((st = check_norm_quant(m, n)) != SK_OK) return st;
+  if ((st = check_ptrs16("sk_gemm_rmsnorm_bf16(x, w, norm_w, z, workspace)",
+                         {x, w, norm_w, z, workspace})) != SK_OK)
+    return st;
+  if (workspace_bytes < sk_gemm_rmsnorm_nvfp4_workspace(m, n))
+    return fail(SK_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes,
+                sk_gemm_rmsnorm_nvfp4_workspace(m, n));
+  sk::DeviceInfo info;
+  if ((st = current_device(&info)) != SK_OK) return st;
+  if ((st = enqueue_gemm(x, w, workspace, m, n, k, splits, stream, info)) != SK_OK) return st;
+  return launch_status(
+      sk::launch_rmsnorm_nvfp4(static_cast<const uint16_t *>(workspace),
+                               static_cast<const uint16_t *>(norm_w), eps, gain_center, nullptr,
+                               nullptr, nullptr, static_cast<uint16_t *>(z), m, n,
+                               as_stream(stream), pdl_enabled()),
+      "rmsnorm_bf16");
+}
+
 sk_status sk_nvfp4_quantize(const void *z, const float *global_scale, uint8_t *a, uint8_t *a_sf,
                             int m, int n, void *stream) {
   sk_status st;

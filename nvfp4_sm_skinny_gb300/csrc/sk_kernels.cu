@@ -390,7 +390,9 @@ __device__ __forceinline__ uint32_t nvfp4_block16(const uint16_t (&z)[16], float
 
 // Pre-expert RMSNorm + NVFP4 (cutedsl/moe/pooler_gather, module docstring;
 // pooler_layer: weight applied after the norm). One CTA per token row; each
-// thread owns one 16-column NVFP4 block.
+// thread owns one 16-column NVFP4 block. With a == NULL the NVFP4 step is
+// skipped and only z is stored: the norm of a BF16 edge layer (same page,
+// module docstring, ExpertsInputBf16).
 __global__ void __launch_bounds__(1024)
     rmsnorm_nvfp4_kernel(const uint16_t *__restrict__ y, const uint16_t *__restrict__ norm_w,
                          float eps, float gc, const float *__restrict__ gs_ptr,
@@ -443,12 +445,13 @@ __global__ void __launch_bounds__(1024)
       const float g = __fadd_rn(bf16_bits_to_f32(w[j]), gc);
       z[j] = bf16_store_bits(__fmul_rn(__fmul_rn(bf16_bits_to_f32(v[j]), r), g));
     }
-    const float gs = *gs_ptr;
-    uint2 packed;
-    const uint32_t sf = nvfp4_block16(z, gs, packed);
     const size_t base = static_cast<size_t>(row) * n + 16 * blk;
-    reinterpret_cast<uint2 *>(a)[base >> 4] = packed;
-    a_sf[base >> 4] = static_cast<uint8_t>(sf);
+    if (a) {  // NVFP4 layers; a BF16 edge layer stores z only
+      uint2 packed;
+      const uint32_t sf = nvfp4_block16(z, *gs_ptr, packed);
+      reinterpret_cast<uint2 *>(a)[base >> 4] = packed;
+      a_sf[base >> 4] = static_cast<uint8_t>(sf);
+    }
     if (z_out) {
       uint16_t lo[8], hi[8];
 #pragma unroll

@@ -127,6 +127,40 @@ def test_pooler_saturates_beyond_calibration(sk):
     assert (sf_tf == 0x7E).any()
 
 
+# ----------------------------------------------------- BF16 edge layers ----
+@pytest.mark.parametrize("m,n", [(1, 4096), (5, 1024), (16, 4096), (3, 16), (2, 16384)])
+def test_rmsnorm_bf16_standalone(sk, m, n):
+    g = torch.Generator().manual_seed(31 * m + n)
+    y = (torch.randn(m, n, generator=g) * 2.0).to(torch.bfloat16)
+    y[0, :] = 0.0 if m > 1 else y[0, :]                 # an all-zero row gives zero rows out
+    nw = (0.1 * torch.randn(n, generator=g)).to(torch.bfloat16)
+    z = sk.rmsnorm_bf16(y.to(DEV), nw.to(DEV), synth.EPS, synth.GAIN_CENTER)
+    torch.cuda.synchronize()
+    z_ref = oracle.rmsnorm_bf16(synth.bits(y), synth.bits(nw), synth.EPS, synth.GAIN_CENTER)
+    assert ulp_distance(synth.bits(z), z_ref).max() <= 1
+    if m > 1:
+        assert torch.all(z[0].view(torch.int16) == 0)
+
+
+@pytest.mark.parametrize("b", [1, 16])
+def test_pooler_edge_layer_bf16(sk, b):
+    d = synth.pooler(b)
+    x, w, nw = d["x"].to(DEV), d["w"].to(DEV), d["norm_w"].to(DEV)
+    z, ws = sk.gemm_rmsnorm_bf16(x, w, nw, d["eps"], d["gain_center"])
+    torch.cuda.synchronize()
+    yb = synth.bits(ws[: b * 4096 * 2].view(torch.bfloat16).view(b, 4096))
+    xb, wb = synth.bits(d["x"]), synth.bits(d["w"])
+    acc, absacc = oracle.gemm_f64(xb, wb)
+    check_gemm(yb, oracle.gemm_bf16(xb, wb), acc, absacc, 8192, sk.gemm_splits(b, 4096, 8192))
+    z_tf = oracle.rmsnorm_bf16(yb, synth.bits(d["norm_w"]), d["eps"], d["gain_center"])
+    assert ulp_distance(synth.bits(z), z_tf).max() <= 1
+    # the same GEMM and norm as the NVFP4 layer's z
+    _, _, z_nv, _ = sk.gemm_rmsnorm_nvfp4(x, w, nw, d["eps"], d["gain_center"], gs_tensor(300.0),
+                                         z_out=True)
+    torch.cuda.synchronize()
+    assert torch.equal(z.view(torch.int16), z_nv.view(torch.int16))
+
+
 # --------------------------------------------------------------- dual norm ----
 def _check_dual(sk, d, p_bits, s0, s_gpu, out_gpu, post_w):
     s_ref, out_ref = oracle.dual_norm(p_bits, s0, None if post_w is None else synth.bits(post_w),
