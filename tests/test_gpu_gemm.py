@@ -1,8 +1,8 @@
 """GPU parity of sk_gemm_bf16 against the CPU oracle (all calls go through the
 C ABI via the binding). Covers exact special cases (identity and one-hot
 weights, zeros), several tiles with a ragged tail, every split count, the
-unpooler shard and the M x (N, K) sweep, padding rows, and bitwise run-to-run
-reproducibility."""
+unpooler shard and the M x (N, K) sweep, the largest shapes (sampled), padding
+rows, and bitwise run-to-run reproducibility."""
 import numpy as np
 import pytest
 import torch
@@ -110,6 +110,18 @@ def test_sweep_m_and_splits(sk, n, k):
             torch.cuda.synchronize()
             s = splits or sk.gemm_splits(m, n, k)
             check_gemm(synth.bits(y), yref, acc, absacc, k, s)
+
+
+@pytest.mark.parametrize("m,n,k", [(16, 24576, 2048), (4, 1024, 32768), (16, 8192, 16384)])
+def test_large_shapes_sampled(sk, m, n, k):
+    # more row tiles than SMs (a second wave), or a long K (many stages, up to
+    # 16 slices); the oracle checks a sample of output features, one in 61
+    x = synth.normal_bf16((m, k), 1.0, 40 + m)
+    w = synth.normal_bf16((n, k), 0.02, 41 + n % 97)
+    y = run(sk, x, w)
+    cols = np.arange(0, n, 61)
+    yref, acc, absacc = ref(x, w[torch.as_tensor(cols)])
+    check_gemm(y[:, cols], yref, acc, absacc, k, sk.gemm_splits(m, n, k))
 
 
 def test_rows_beyond_m_are_not_written(sk):
