@@ -61,6 +61,7 @@ typedef enum sk_status {
 #define SK_DEVICE_WAIT_MMA 0x2u      /* tensor-core stage never filled      */
 #define SK_DEVICE_WAIT_EPILOGUE 0x4u /* accumulator never completed         */
 #define SK_DEVICE_WAIT_GRID 0x8u     /* a grid-wide barrier never completed  */
+#define SK_DEVICE_WAIT_PROBE 0x10u   /* sk_wait_probe's wait ran out (expected) */
 
 /* Message of the last failed call on this host thread ("" if none). The
    string lives in thread-local storage owned by the library. */
@@ -273,6 +274,16 @@ sk_status sk_gemm_rmsnorm_nvfp4_static(const void *x, const void *w, const void 
                                        float eps, float gain_center, const float *global_scale,
                                        uint8_t *a, uint8_t *a_sf, void *z_out, int m, int n,
                                        int k, int splits, void *stream);
+
+/*
+ * sk_wait_probe -- diagnostic of the bounded-wait path: launches one CTA that
+ * waits on an mbarrier that nothing completes, through the same bounded wait
+ * the kernels use, for at most limit_us microseconds (1 <= limit_us <=
+ * 100000). When the wait runs out the kernel sets SK_DEVICE_WAIT_PROBE in the
+ * device status word and returns; the context stays usable. No counterpart
+ * on the pages: it tests this library's failure reporting without a fault.
+ */
+sk_status sk_wait_probe(unsigned limit_us, void *stream);
 
 /*
  * sk_device_status -- HOST-synchronizing diagnostic: copies the library's

@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
                                  vp, f, f, f, f, f, f, vp, sz, i, i, i, i, vp], i),
             "sk_device_status": ([ctypes.POINTER(ctypes.c_uint32), i], i),
             "sk_convert_probe": ([i, vp, vp, i, vp], i),
+            "sk_wait_probe": ([ctypes.c_uint, vp], i),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -382,6 +383,15 @@ def device_status(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _check(lib().sk_device_status(ctypes.byref(v), 1 if clear else 0))
     return int(v.value)
+
+
+SK_DEVICE_WAIT_PROBE = 0x10
+
+
+def wait_probe(limit_us: int, stream=None) -> None:
+    """Launches a kernel whose bounded wait is meant to run out after limit_us
+    microseconds; it sets SK_DEVICE_WAIT_PROBE in the device status word."""
+    _check(lib().sk_wait_probe(limit_us, _stream(stream)))
 
 
 def convert_probe(kind: int, inp: torch.Tensor, stream=None) -> torch.Tensor:

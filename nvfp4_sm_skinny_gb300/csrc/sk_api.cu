@@ -567,6 +567,16 @@ sk_status sk_decode_layer(const void *h_in, const void *w_o, const void *w_p, co
                        "decode_layer");
 }
 
+sk_status sk_wait_probe(unsigned limit_us, void *stream) {
+  if (limit_us < 1 || limit_us > 100000)
+    return fail(SK_ERR_INVALID_ARG, "limit_us=%u: needs 1 <= limit_us <= 100000", limit_us);
+  sk::DeviceInfo info;
+  sk_status st;
+  if ((st = current_device(&info)) != SK_OK) return st;
+  return launch_status(sk::launch_wait_probe(static_cast<uint64_t>(limit_us) * 1000, as_stream(stream)),
+                       "wait_probe");
+}
+
 sk_status sk_device_status(uint32_t *out, int clear) {
   if (!out) return fail(SK_ERR_INVALID_ARG, "out is null");
   sk::DeviceInfo info;

@@ -125,6 +125,8 @@ cudaError_t launch_dual_norm(const uint16_t *p, float *s, const uint16_t *w1, fl
 
 cudaError_t launch_convert_probe(int kind, const void *in, void *out, int n, cudaStream_t stream);
 
+cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t stream);
+
 cudaError_t read_device_status(uint32_t *out, bool clear);
 
 // Fused decode layer (sk_decode.cuh): arguments, layout, launch.

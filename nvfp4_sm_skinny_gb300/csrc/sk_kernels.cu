@@ -583,6 +583,17 @@ __global__ void __launch_bounds__(kDualThreads)
 }
 
 
+// Waits on an mbarrier nothing completes, for at most limit_ns, with the
+// bounded wait the kernels use; reports the expected timeout in the status word.
+__global__ void wait_probe_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+    if (!mbar_wait_bounded(smem_u32(&bar), 0, limit_ns)) atomicOr(&g_device_status, SK_DEVICE_WAIT_PROBE);
+  }
+}
+
 // Format-conversion probe over n inputs (see sk_convert_probe).
 __global__ void convert_probe_kernel(int kind, const void *__restrict__ in, void *__restrict__ out,
                                      int n) {
@@ -765,6 +776,11 @@ cudaError_t launch_dual_norm(const uint16_t *p, float *s, const uint16_t *w1, fl
   const int threads = (h / 8 + 31) / 32 * 32;
   return launch_ex(dual_norm_kernel, dim3(1, m), dim3(threads), 0, stream, pdl, dim3(1, 1, 1), p, s,
                    w1, alpha, beta, w2, out, eps_post, eps_pre, gc_post, gc_pre, h);
+}
+
+cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_convert_probe(int kind, const void *in, void *out, int n, cudaStream_t stream) {
