@@ -237,6 +237,17 @@ def test_nvfp4_exactly_representable_roundtrip(oracle_mod):
         assert np.array_equal(unpacked, codes)
 
 
+def test_nvfp4_zero_blocks_give_zero_scale_and_codes(oracle_mod):
+    # an all-zero block: amax = 0, sf = 0x00, os = 0 and every code 0x0 (z is
+    # canonical +0); a zero block next to a non-zero one is unaffected by it
+    z = np.zeros((3, 64), np.float32)
+    z[1, 16:32] = 1.5
+    a, a_sf = oracle_mod.nvfp4_quantize(bf16_bits(z), 100.0)
+    assert np.all(a_sf[0] == 0) and np.all(a[0] == 0) and np.all(a[2] == 0)
+    assert a_sf[1, 0] == 0 and a_sf[1, 2] == 0 and a_sf[1, 3] == 0 and a_sf[1, 1] != 0
+    assert np.all(a[1, :8] == 0) and np.all(a[1, 16:] == 0) and np.all(a[1, 8:16] == 0x77)
+
+
 def test_nvfp4_constant_row_same_code_every_block(oracle_mod):
     z = bf16_bits(np.full((2, 256), -1.375, np.float32))
     a, a_sf = oracle_mod.nvfp4_quantize(z, 37.0)
