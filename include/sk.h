@@ -100,6 +100,24 @@ sk_status sk_gemm_bf16(const void *x, const void *w, void *y, int m, int n, int 
                        int splits, void *stream);
 
 /*
+ * sk_gemm_prefetch_next -- a hint for the next GEMM that this host thread
+ * enqueues (sk_gemm_bf16, sk_gemm_rmsnorm_nvfp4, sk_gemm_rmsnorm_bf16,
+ * sk_gemm_dual_norm): once each of its CTAs has issued the copies of its own
+ * weight slice, it starts towards L2 the first weight stages of the GEMM
+ * y' = x' @ w_next^T (w_next BF16 [n_next, k_next], automatic splits) that
+ * follows it in the stream, so that HBM keeps streaming through the first
+ * GEMM's drain and epilogue, whatever runs between the two, and the second's
+ * launch. No counterpart on the pages (there, each call streams only its own
+ * weight). Results are unchanged; only timing depends on the hint.
+ *   w_next 16-byte aligned, (n_next, k_next) a supported GEMM shape;
+ *   w_next NULL clears a pending hint. The next GEMM enqueue on this thread
+ *   consumes the hint (thread-local state); a call that fails before its GEMM
+ *   is enqueued leaves it pending. A hint whose GEMM is later run with explicit
+ *   splits other than the automatic ones warms the wrong tiles: still correct.
+ */
+sk_status sk_gemm_prefetch_next(const void *w_next, int n_next, int k_next);
+
+/*
  * sk_rmsnorm_nvfp4 -- pre-expert RMSNorm of a BF16 [m, n] input, then NVFP4
  * (cutedsl/moe/pooler_gather: module docstring, PoolerLayer, pooler_layer,
  * nvfp4_compute_output_scale, cvt_e2m1x8_f32, cvt_f32_to_e4m3).

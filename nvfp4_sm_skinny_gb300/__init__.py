@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
             "sk_gemm_splits": ([i, i, i, i], i),
             "sk_gemm_supported": ([i, i, i, i], i),
             "sk_gemm_bf16": ([vp, vp, vp, i, i, i, i, vp], i),
+            "sk_gemm_prefetch_next": ([vp, i, i], i),
             "sk_rmsnorm_nvfp4": ([vp, vp, f, f, vp, vp, vp, vp, i, i, vp], i),
             "sk_gemm_rmsnorm_nvfp4_workspace": ([i, i], sz),
             "sk_gemm_rmsnorm_nvfp4": ([vp, vp, vp, f, f, vp, vp, vp, vp, vp, sz, i, i, i, i, vp], i),
@@ -152,6 +153,18 @@ def gemm_bf16(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None,
     _need(out, torch.bfloat16, (m, n), "out")
     _check(lib().sk_gemm_bf16(_ptr(x), _ptr(w), _ptr(out), m, n, k, splits, _stream(stream)))
     return out
+
+
+def gemm_prefetch_next(w_next: torch.Tensor | None) -> None:
+    """Hint for the next GEMM this thread enqueues: once it has issued its own
+    weight copies, it starts the first weight stages of the GEMM with weight
+    ``w_next`` [n, k] (BF16) towards L2. ``None`` clears the hint."""
+    if w_next is None:
+        _check(lib().sk_gemm_prefetch_next(None, 0, 0))
+        return
+    _need(w_next, torch.bfloat16, tuple(w_next.shape), "w_next")
+    n, k = w_next.shape
+    _check(lib().sk_gemm_prefetch_next(_ptr(w_next), n, k))
 
 
 # -------------------------------------------------------- RMSNorm + NVFP4 ----

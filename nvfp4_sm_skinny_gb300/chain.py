@@ -46,8 +46,11 @@ class DecodeChain:
     """Weights and buffers of an L-layer chain at M rows on one device."""
 
     def __init__(self, layers: int = 48, m: int = 16, device="cuda", eps: float = synth.EPS,
-                 gain_center: float = synth.GAIN_CENTER, splits: int = 0):
+                 gain_center: float = synth.GAIN_CENTER, splits: int = 0,
+                 prefetch_next: bool = True):
         self.L, self.m, self.device = layers, m, torch.device(device)
+        # each GEMM starts the next GEMM's first weight stages towards L2
+        self.prefetch_next = prefetch_next
         self.eps, self.gc, self.splits = eps, gain_center, splits
         dev = self.device
         self.w_o, self.w_p, self.w_u = [], [], []
@@ -103,8 +106,18 @@ class DecodeChain:
             sk.gemm_bf16(self.z[l], self.w_u[l], out=self.h[l + 1], splits=self.splits,
                          stream=stream)
 
+    def next_weight(self, l: int, op: int):
+        """The weight of the GEMM after layer l's call `op` (None after the last)."""
+        if op == 0:
+            return self.w_p[l]
+        if op == 1:
+            return self.w_u[l]
+        return self.w_o[l + 1] if l + 1 < self.L else None
+
     def layer(self, l: int, stream=None) -> None:
         for op in range(3):
+            if self.prefetch_next:
+                sk.gemm_prefetch_next(self.next_weight(l, op))
             self.layer_op(l, op, stream)
 
     def forward(self, stream=None) -> None:
@@ -128,11 +141,15 @@ class DecodeChain:
     def gemms_only(self, stream=None) -> None:
         """The chain's three GEMMs per layer without their epilogues (same
         shapes, weights and launch configuration), for timing the GEMM kernel."""
+        hint = sk.gemm_prefetch_next if self.prefetch_next else (lambda w: None)
         for l in range(self.L):
+            hint(self.next_weight(l, 0))
             sk.gemm_bf16(self.h[l], self.w_o[l], out=self.ws_o[l][: self.m * H * 2].view(
                 torch.bfloat16).view(self.m, H), splits=self.splits, stream=stream)
+            hint(self.next_weight(l, 1))
             sk.gemm_bf16(self.u[l], self.w_p[l], out=self.ws_p[l][: self.m * P * 2].view(
                 torch.bfloat16).view(self.m, P), splits=self.splits, stream=stream)
+            hint(self.next_weight(l, 2))
             sk.gemm_bf16(self.z[l], self.w_u[l], out=self.h[l + 1], splits=self.splits,
                          stream=stream)
 

@@ -206,9 +206,43 @@ sk_status launch_status(cudaError_t e, const char *what) {
   return ok();
 }
 
+// The weight of the GEMM this host thread enqueues after the next one
+// (sk_gemm_prefetch_next); consumed by the next GEMM enqueue. t_prefetched:
+// the weight whose first stages the last GEMM enqueue started towards L2.
+struct PrefetchHint {
+  const void *w = nullptr;
+  int n = 0, k = 0;
+  bool operator==(const PrefetchHint &o) const { return w == o.w && n == o.n && k == o.k; }
+};
+thread_local PrefetchHint t_prefetch;
+thread_local PrefetchHint t_prefetched;
+
+// Stages of the next GEMM's slice that each of its CTAs has started towards
+// L2 by the previous GEMM: about 448 KiB per CTA, at most 64 MiB in all
+// (measured best on the decode chain, where this GEMM's own look-ahead is then
+// left out; more slows the norm kernels between the GEMMs). SK_PF_STAGES
+// overrides (0: none).
+int prefetch_stages(const GemmPlan &next, int tiles) {
+  const char *v = std::getenv("SK_PF_STAGES");
+  if (v && *v) {
+    const int n = std::atoi(v);
+    return n < 0 ? 0 : (n > 64 ? 64 : n);
+  }
+  const long stage_w = static_cast<long>(next.bps) * next.h * 128;
+  const long per_cta = (448L * 1024 + stage_w - 1) / stage_w;
+  const long cap = (64L << 20) / (stage_w * tiles * next.splits);
+  return static_cast<int>(std::max(1L, std::min(per_cta, cap)));
+}
+
 // Validated GEMM enqueue shared by the three GEMM entry points.
 sk_status enqueue_gemm(const void *x, const void *w, void *y, int m, int n, int k, int splits,
                        void *stream, const sk::DeviceInfo &info) {
+  const PrefetchHint hint = t_prefetch;
+  // this GEMM's first weight stages were started by the previous one: no
+  // look-ahead of its own
+  const bool warmed = t_prefetched.w && t_prefetched == PrefetchHint{w, n, k};
+  t_prefetch = PrefetchHint{};
+  t_prefetched = PrefetchHint{};
   int dev = 0;
   cudaGetDevice(&dev);
   const GemmPlan plan = plan_gemm(n, k, splits, dev, info.sm_count);
@@ -218,10 +252,27 @@ sk_status enqueue_gemm(const void *x, const void *w, void *y, int m, int n, int 
   sk_status st;
   if ((st = make_map(&tw, w, n, k, plan.h, plan.bps)) != SK_OK) return st;
   if ((st = make_map(&tx, x, m, k, sk::kTokTile, plan.bps)) != SK_OK) return st;
-  return launch_status(sk::launch_gemm(tw, tx, static_cast<uint16_t *>(y), m, n, k, plan.splits,
-                                       plan.h, plan.stages, plan.bps, as_stream(stream),
-                                       pdl_enabled()),
-                       "gemm");
+  sk::GemmPrefetch pf;
+  const sk::GemmPrefetch *pfp = nullptr;
+  if (hint.w) {
+    const GemmPlan np = plan_gemm(hint.n, hint.k, 0, dev, info.sm_count);
+    pf.stages = np.splits ? prefetch_stages(np, (hint.n + np.h - 1) / np.h) : 0;
+    if (pf.stages > 0) {
+      if ((st = make_map(&pf.map, hint.w, hint.n, hint.k, np.h, np.bps)) != SK_OK) return st;
+      pf.h = np.h;
+      pf.nkb = hint.k / sk::kBlockK / np.splits;
+      pf.bps = np.bps;
+      pf.tiles = (hint.n + np.h - 1) / np.h;
+      pf.splits = np.splits;
+      pfp = &pf;
+    }
+  }
+  st = launch_status(sk::launch_gemm(tw, tx, static_cast<uint16_t *>(y), m, n, k, plan.splits,
+                                     plan.h, plan.stages, plan.bps, as_stream(stream),
+                                     pdl_enabled(), pfp, warmed ? 0 : -1),
+                     "gemm");
+  if (st == SK_OK && pfp) t_prefetched = hint;
+  return st;
 }
 
 sk_status check_ptrs16(const char *names, std::initializer_list<const void *> ps) {
@@ -281,6 +332,18 @@ sk_status sk_gemm_bf16(const void *x, const void *w, void *y, int m, int n, int 
   sk::DeviceInfo info;
   if ((st = current_device(&info)) != SK_OK) return st;
   return enqueue_gemm(x, w, y, m, n, k, splits, stream, info);
+}
+
+sk_status sk_gemm_prefetch_next(const void *w_next, int n_next, int k_next) {
+  if (!w_next) {
+    t_prefetch = PrefetchHint{};
+    return ok();
+  }
+  sk_status st;
+  if ((st = check_gemm_shape(1, n_next, k_next, 0)) != SK_OK) return st;
+  if ((st = check_ptrs16("sk_gemm_prefetch_next(w_next)", {w_next})) != SK_OK) return st;
+  t_prefetch = PrefetchHint{w_next, n_next, k_next};
+  return ok();
 }
 
 static sk_status check_norm_quant(int m, int n) {

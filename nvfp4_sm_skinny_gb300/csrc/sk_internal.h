@@ -105,11 +105,23 @@ size_t gemm_smem_bytes(int h, int stages, int bps, int splits);
 // once with `ctas_per_sm` (1 or 2) GEMM CTAs per SM (cached).
 int gemm_max_clusters(int device, int splits, int ctas_per_sm);
 
+// The GEMM enqueued next, whose first weight stages a GEMM launch starts
+// towards L2 once it has issued its own last weight copy: its weight map (3-D,
+// box {64, h, bps}), tile height, K blocks per split, boxes per stage, row
+// tiles and splits, and how many of its stages to start per CTA.
+struct GemmPrefetch {
+  CUtensorMap map;
+  int h, nkb, bps, tiles, splits, stages;
+};
+
 // Launches the split-K GEMM: grid (ceil(n / h), splits), cluster
 // (1, splits, 1); tile height h rows, `stages` pipeline stages of `bps` boxes.
+// pf (may be null): the next GEMM's weights to start towards L2. l2_ahead:
+// own weight stages beyond the ring started towards L2 before the dependency
+// wait (-1: about 256 KiB).
 cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, uint16_t *y, int m,
                         int n, int k, int splits, int h, int stages, int bps, cudaStream_t stream,
-                        bool pdl);
+                        bool pdl, const GemmPrefetch *pf = nullptr, int l2_ahead = -1);
 
 cudaError_t launch_rmsnorm_nvfp4(const uint16_t *y, const uint16_t *norm_w, float eps, float gc,
                                  const float *gs, uint8_t *a, uint8_t *a_sf, uint16_t *z_out,

@@ -38,6 +38,12 @@ struct GemmArgs {
   int bps;           // boxes per stage
   int splits;
   int l2_ahead;      // weight stages started towards L2 before the dependency wait
+  // The GEMM enqueued after this one (tensor map tmap_pf): once this CTA has
+  // issued its last weight copy, it starts towards L2 the first pf_stages
+  // stages of the next GEMM's CTAs c, c + ctas, ... (c = this CTA's linear
+  // index). pf_stages = 0: nothing.
+  int pf_stages;
+  int pf_h, pf_nkb, pf_bps, pf_tiles, pf_ctas;
 };
 
 // Bounded wait that also gives up as soon as another role raised `abort`.
@@ -83,7 +89,7 @@ __device__ __forceinline__ void store_tile_rows(uint16_t *stage, const float (&v
 // per thread).
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
-                GemmArgs args) {
+                const __grid_constant__ CUtensorMap tmap_pf, GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -177,6 +183,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tma_load_3d(smem_u32(s_w + s * B * slot_w), &tmap_w, full0 + 8 * s, 0, n0, kb, pol_w);
       tma_load_3d(smem_u32(s_x + s * B * kSlotXBytes), &tmap_x, full0 + 8 * s, 0, 0, kb, pol_x);
       issued = i + 1;
+    }
+    // Once this CTA's last stage has landed, HBM would idle here through the
+    // epilogue, whatever runs in between and the next launch: start the next
+    // GEMM's first weight stages towards L2. (Issued any earlier, these copies
+    // delay the last stages of this GEMM, which every later kernel waits for.)
+    if (args.pf_stages > 0 && !*abort_flag && issued > 0 &&
+        mbar_wait_bounded(full0 + 8 * ((issued - 1) % stages), ((issued - 1) / stages) & 1,
+                          kWaitLimitNs)) {
+      const int ctas = static_cast<int>(gridDim.x * gridDim.y);
+      for (int c = static_cast<int>(blockIdx.x + blockIdx.y * gridDim.x); c < args.pf_ctas; c += ctas) {
+        const int pn0 = (c % args.pf_tiles) * args.pf_h;
+        const int pkb0 = (c / args.pf_tiles) * args.pf_nkb;
+        for (int j = 0; j < args.pf_stages && j * args.pf_bps < args.pf_nkb; ++j)
+          tma_prefetch_l2_3d(&tmap_pf, 0, pn0, pkb0 + j * args.pf_bps);
+      }
     }
   } else if (warp >= 1 && warp <= kGemmIssuers && lane == 0) {
     // ---------------------------------------------------- MMA issuers
@@ -723,9 +744,9 @@ int gemm_max_clusters(int device, int splits, int ctas_per_sm) {
 
 cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, uint16_t *y, int m,
                         int n, int k, int splits, int h, int stages, int bps,
-                        cudaStream_t stream, bool pdl) {
+                        cudaStream_t stream, bool pdl, const GemmPrefetch *pf, int l2_ahead) {
   if (h % 8 || h < 8 || h > kMmaM || bps < 1 || bps > kMaxBoxesPerStage) return cudaErrorInvalidValue;
-  GemmArgs a;
+  GemmArgs a = {};
   a.y = y;
   a.m = m;
   a.n = n;
@@ -735,19 +756,31 @@ cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, ui
   a.bps = bps;
   a.splits = splits;
   // Weight stages started towards L2 before the dependency wait, beyond the
-  // ring: about 256 KiB per CTA (measured best on the decode chain: the
-  // previous kernel's tail and the norm between two GEMMs leave HBM idle;
-  // much more slows that norm's own memory accesses). SK_L2_AHEAD overrides.
+  // ring: by default about 256 KiB per CTA (measured best for GEMMs that
+  // follow one another: the previous kernel's tail leaves HBM idle; much
+  // more slows the memory accesses of a norm kernel between two GEMMs), or
+  // what the caller says (l2_ahead >= 0). SK_L2_AHEAD overrides both.
   {
     const char *v = std::getenv("SK_L2_AHEAD");
     const int stage_w = bps * h * 128;
-    a.l2_ahead = v ? std::atoi(v) : (256 * 1024 + stage_w - 1) / stage_w;
+    a.l2_ahead = v ? std::atoi(v) : l2_ahead >= 0 ? l2_ahead : (256 * 1024 + stage_w - 1) / stage_w;
     if (a.l2_ahead < 0) a.l2_ahead = 0;
     if (a.l2_ahead > 64) a.l2_ahead = 64;
   }
+  if (pf && pf->stages > 0) {
+    if (pf->h % 8 || pf->h < 8 || pf->h > kMmaM || pf->bps < 1 || pf->bps > kMaxBoxesPerStage ||
+        pf->tiles < 1 || pf->splits < 1 || pf->nkb < 1)
+      return cudaErrorInvalidValue;
+    a.pf_stages = pf->stages;
+    a.pf_h = pf->h;
+    a.pf_nkb = pf->nkb;
+    a.pf_bps = pf->bps;
+    a.pf_tiles = pf->tiles;
+    a.pf_ctas = pf->tiles * pf->splits;
+  }
   const dim3 grid((n + h - 1) / h, splits, 1);
   return launch_ex(gemm_kernel, grid, dim3(kGemmThreads), gemm_smem_bytes(h, stages, bps, splits), stream, pdl,
-                   dim3(1, splits, 1), tmap_w, tmap_x, a);
+                   dim3(1, splits, 1), tmap_w, tmap_x, a.pf_stages ? pf->map : tmap_w, a);
 }
 
 cudaError_t launch_rmsnorm_nvfp4(const uint16_t *y, const uint16_t *norm_w, float eps, float gc,

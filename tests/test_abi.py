@@ -85,6 +85,19 @@ def test_pointer_validation(sk):
     assert lib.sk_gemm_dual_norm_workspace(3, 8192) == (3 * 8192 * 2 + 255) // 256 * 256
 
 
+def test_prefetch_hint_validation(sk):
+    # the hint is host state only: it is checked and stored without CUDA
+    lib = sk.lib()
+    vp = ctypes.c_void_p
+    assert lib.sk_gemm_prefetch_next(None, 0, 0) == 0          # clears
+    assert lib.sk_gemm_prefetch_next(vp(P), 24, 64) == 1        # n not a multiple of 16
+    assert lib.sk_gemm_prefetch_next(vp(P), 128, 96) == 1       # k not a multiple of 64
+    assert lib.sk_gemm_prefetch_next(vp(P + 8), 128, 64) == 1
+    assert "aligned" in sk.last_error()
+    assert lib.sk_gemm_prefetch_next(vp(P), 128, 64) == 0
+    assert lib.sk_gemm_prefetch_next(None, 0, 0) == 0
+
+
 def test_epilogue_validation(sk):
     lib = sk.lib()
     vp = ctypes.c_void_p

@@ -102,3 +102,25 @@ def test_graph_replay_equals_eager(chain):
         assert torch.equal(c.h[c.L].view(torch.int16), eager[0].view(torch.int16))
         assert torch.equal(c.a, eager[1]) and torch.equal(c.a_sf, eager[2])
         assert torch.equal(c.s, eager[3])
+
+
+def test_prefetch_hints_leave_the_chain_unchanged(chain):
+    # forward() hints each GEMM with the next GEMM's weight; without the hints
+    # every result is the same, bit for bit
+    c = chain
+    assert c.prefetch_next
+    c.set_input(c.h0, c.s0)
+    c.forward()
+    torch.cuda.synchronize()
+    hinted = (c.h[c.L].clone(), c.a.clone(), c.a_sf.clone(), c.s.clone(), c.u.clone())
+    c.prefetch_next = False
+    try:
+        c.set_input(c.h0, c.s0)
+        c.forward()
+        torch.cuda.synchronize()
+    finally:
+        c.prefetch_next = True
+    assert torch.equal(c.h[c.L].view(torch.int16), hinted[0].view(torch.int16))
+    assert torch.equal(c.a, hinted[1]) and torch.equal(c.a_sf, hinted[2])
+    assert torch.equal(c.s, hinted[3])
+    assert torch.equal(c.u.view(torch.int16), hinted[4].view(torch.int16))

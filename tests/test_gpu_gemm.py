@@ -124,6 +124,31 @@ def test_large_shapes_sampled(sk, m, n, k):
     check_gemm(y[:, cols], yref, acc, absacc, k, sk.gemm_splits(m, n, k))
 
 
+@pytest.mark.parametrize("n2,k2", [(4096, 8192), (1024, 512)])
+def test_prefetch_hint_leaves_results_unchanged(sk, n2, k2):
+    # A GEMM told which weight comes next starts that weight's first stages
+    # towards L2 after its own last copy; the next GEMM then skips its own
+    # look-ahead. Neither result may change, including when the hinted shape
+    # is not the one that follows.
+    x = synth.gemm_x(16, 4096).to(DEV)
+    w = synth.gemm_weight(8192, 4096).to(DEV)
+    w2 = synth.gemm_weight(n2, k2, 1).to(DEV)
+    x2 = synth.gemm_x(16, k2).to(DEV)
+    y_ref = sk.gemm_bf16(x, w)
+    y2_ref = sk.gemm_bf16(x2, w2)
+    for _ in range(3):
+        sk.gemm_prefetch_next(w2)
+        y = sk.gemm_bf16(x, w)
+        y2 = sk.gemm_bf16(x2, w2)            # its first stages were warmed
+        sk.gemm_prefetch_next(w)             # a hint that does not match what follows
+        y3 = sk.gemm_bf16(x2, w2)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+        assert torch.equal(y2.view(torch.int16), y2_ref.view(torch.int16))
+        assert torch.equal(y3.view(torch.int16), y2_ref.view(torch.int16))
+    sk.gemm_prefetch_next(None)
+
+
 def test_rows_beyond_m_are_not_written(sk):
     m, n, k = 5, 256, 256
     x = synth.normal_bf16((m, k), 1.0, 30)
