@@ -488,6 +488,16 @@ def run_sweep(args, local):
         rows.append(r)
         print(json.dumps(r), flush=True)
 
+    def hinted(ws, call):
+        """The same calls, each told the next call's weight (sk_gemm_prefetch_next;
+        the last one the first's, for the next replay)."""
+        def one(i):
+            def f():
+                sk.gemm_prefetch_next(ws[(i + 1) % len(ws)])
+                call(ws[i])
+            return f
+        return [one(i) for i in range(len(ws))]
+
     # GEMM (the unpooler shard and the sweep)
     for n, k in ((1024, 4096), (8192, 4096)):
         ws = [synth.gemm_weight(n, k, i, device=dev) for i in range(copies)]
@@ -501,6 +511,9 @@ def run_sweep(args, local):
                                 for w in ws])
                 record("gemm", m, n, k, S if S else f"auto({sk.gemm_splits(m, n, k)})", sec,
                        2 * n * k + 2 * m * k + 2 * m * n)
+            sec = per_call(hinted(ws, lambda w: sk.gemm_bf16(x, w, out=y, stream=stream)))
+            record("gemm, next weight hinted", m, n, k, f"auto({sk.gemm_splits(m, n, k)})", sec,
+                   2 * n * k + 2 * m * k + 2 * m * n)
         del ws
         torch.cuda.empty_cache()
     # pooler GEMM + pre-expert RMSNorm + NVFP4
@@ -517,6 +530,11 @@ def run_sweep(args, local):
                                                           a=a, a_sf=a_sf, workspace=wsp, stream=stream)
                         for w in ws])
         record("pooler+rmsnorm+nvfp4", b, P, H, f"auto({sk.gemm_splits(b, P, H)})", sec,
+               2 * P * H + 2 * b * H + 2 * P + 4 + b * P // 2 + b * P // 16)
+        sec = per_call(hinted(ws, lambda w: sk.gemm_rmsnorm_nvfp4(
+            x, w, nw, synth.EPS, synth.GAIN_CENTER, gs, a=a, a_sf=a_sf, workspace=wsp, stream=stream)))
+        record("pooler+rmsnorm+nvfp4, next weight hinted", b, P, H,
+               f"auto({sk.gemm_splits(b, P, H)})", sec,
                2 * P * H + 2 * b * H + 2 * P + 4 + b * P // 2 + b * P // 16)
     del ws
     torch.cuda.empty_cache()
@@ -537,6 +555,12 @@ def run_sweep(args, local):
                         for w in ws])
         record("oproj+dual_norm", b, H, K, f"auto({sk.gemm_splits(b, H, K)})", sec,
                2 * H * K + 2 * b * K + 3 * 2 * H + 2 * 4 * b * H + 2 * b * H)
+        sec = per_call(hinted(ws, lambda w: sk.gemm_dual_norm(
+            x, w, s_res, post_w, 1.0, beta, pre_w, out=out, eps_post=synth.EPS, eps_pre=synth.EPS,
+            workspace=wsp, stream=stream)))
+        record("oproj+dual_norm, next weight hinted", b, H, K, f"auto({sk.gemm_splits(b, H, K)})",
+               sec, 2 * H * K + 2 * b * K + 3 * 2 * H + 2 * 4 * b * H + 2 * b * H)
+    sk.gemm_prefetch_next(None)
     print(f"\n| workload | M | N | K | splits | µs/call | GB/s | % of {peak_src} peak ({peak:.0f} GB/s) |")
     print("|---|---|---|---|---|---|---|---|")
     for r in rows:
