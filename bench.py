@@ -514,6 +514,13 @@ def run_sweep(args, local):
             sec = per_call(hinted(ws, lambda w: sk.gemm_bf16(x, w, out=y, stream=stream)))
             record("gemm, next weight hinted", m, n, k, f"auto({sk.gemm_splits(m, n, k)})", sec,
                    2 * n * k + 2 * m * k + 2 * m * n)
+            # x is written by no kernel here (one host copy, synchronised): the
+            # calls may read it without waiting for the call ahead of them
+            torch.cuda.synchronize(dev)
+            sec = per_call(hinted(ws, lambda w: sk.gemm_bf16(x, w, out=y, stream=stream,
+                                                             x_ready=True)))
+            record("gemm, x ready, next weight hinted", m, n, k,
+                   f"auto({sk.gemm_splits(m, n, k)})", sec, 2 * n * k + 2 * m * k + 2 * m * n)
         del ws
         torch.cuda.empty_cache()
     # pooler GEMM + pre-expert RMSNorm + NVFP4

@@ -99,6 +99,30 @@ sk_status sk_gemm_supported(int m, int n, int k, int splits);
 sk_status sk_gemm_bf16(const void *x, const void *w, void *y, int m, int n, int k,
                        int splits, void *stream);
 
+/* Flags of sk_gemm_bf16_ex. */
+#define SK_GEMM_X_READY 0x1u /* no kernel still running may write x */
+
+/*
+ * sk_gemm_bf16_ex -- sk_gemm_bf16 with flags. This library's kernels start
+ * before the kernel ahead of them on the stream has finished (programmatic
+ * dependent launch): they stream their weights at once, read their
+ * activations only after that kernel completes, and complete only after it.
+ * With SK_GEMM_X_READY the GEMM reads x at once as well; only its stores of y
+ * wait, so y is still written in stream order. The caller promises that no
+ * kernel that writes x can still be running when the GEMM starts. That holds
+ * when x was written by host copies only, or by kernels that precede a copy,
+ * an event wait, a launch without programmatic dependent launch, or a host
+ * synchronisation on this stream. It does not hold for a kernel just ahead in
+ * a chain of this library's calls, nor for any call that chain reaches back
+ * to. A run of GEMMs on one such input (rotated weights, several projections
+ * of the same activations) then overlaps call with call. No counterpart on the
+ * pages: there, activations are always read after the wait (unpooler page,
+ * module docstring). Results are those of sk_gemm_bf16, bit for bit.
+ *   flags: 0 or SK_GEMM_X_READY; other bits are rejected (SK_ERR_INVALID_ARG).
+ */
+sk_status sk_gemm_bf16_ex(const void *x, const void *w, void *y, int m, int n, int k,
+                          int splits, unsigned flags, void *stream);
+
 /*
  * sk_gemm_prefetch_next -- a hint for the next GEMM that this host thread
  * enqueues (sk_gemm_bf16, sk_gemm_rmsnorm_nvfp4, sk_gemm_rmsnorm_bf16,

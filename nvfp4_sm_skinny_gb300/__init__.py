@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
             "sk_gemm_supported": ([i, i, i, i], i),
             "sk_gemm_bf16": ([vp, vp, vp, i, i, i, i, vp], i),
             "sk_gemm_prefetch_next": ([vp, i, i], i),
+            "sk_gemm_bf16_ex": ([vp, vp, vp, i, i, i, i, ctypes.c_uint, vp], i),
             "sk_rmsnorm_nvfp4": ([vp, vp, f, f, vp, vp, vp, vp, i, i, vp], i),
             "sk_gemm_rmsnorm_nvfp4_workspace": ([i, i], sz),
             "sk_gemm_rmsnorm_nvfp4": ([vp, vp, vp, f, f, vp, vp, vp, vp, vp, sz, i, i, i, i, vp], i),
@@ -141,9 +142,16 @@ def gemm_splits(m: int, n: int, k: int, splits: int = 0) -> int:
 
 
 # ----------------------------------------------------------------- GEMM ----
+GEMM_X_READY = 0x1
+
+
 def gemm_bf16(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None,
-              splits: int = 0, stream=None) -> torch.Tensor:
-    """out[m, n] = x[m, k] @ w[n, k]^T (BF16 in/out, FP32 accumulate)."""
+              splits: int = 0, stream=None, x_ready: bool = False) -> torch.Tensor:
+    """out[m, n] = x[m, k] @ w[n, k]^T (BF16 in/out, FP32 accumulate).
+    ``x_ready``: no kernel that writes x can still be running when this GEMM
+    starts (x written by host copies, or by kernels before a copy, event wait,
+    non-overlapped launch or synchronisation), so the GEMM reads it without
+    waiting for the kernel ahead of it (sk_gemm_bf16_ex, SK_GEMM_X_READY)."""
     m, k = x.shape
     n = w.shape[0]
     _need(x, torch.bfloat16, (m, k), "x")
@@ -151,7 +159,11 @@ def gemm_bf16(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None,
     if out is None:
         out = torch.empty(m, n, dtype=torch.bfloat16, device=x.device)
     _need(out, torch.bfloat16, (m, n), "out")
-    _check(lib().sk_gemm_bf16(_ptr(x), _ptr(w), _ptr(out), m, n, k, splits, _stream(stream)))
+    if x_ready:
+        _check(lib().sk_gemm_bf16_ex(_ptr(x), _ptr(w), _ptr(out), m, n, k, splits, GEMM_X_READY,
+                                     _stream(stream)))
+    else:
+        _check(lib().sk_gemm_bf16(_ptr(x), _ptr(w), _ptr(out), m, n, k, splits, _stream(stream)))
     return out
 
 

@@ -236,7 +236,7 @@ int prefetch_stages(const GemmPlan &next, int tiles) {
 
 // Validated GEMM enqueue shared by the three GEMM entry points.
 sk_status enqueue_gemm(const void *x, const void *w, void *y, int m, int n, int k, int splits,
-                       void *stream, const sk::DeviceInfo &info) {
+                       void *stream, const sk::DeviceInfo &info, bool x_ready = false) {
   const PrefetchHint hint = t_prefetch;
   // this GEMM's first weight stages were started by the previous one: no
   // look-ahead of its own
@@ -269,7 +269,7 @@ sk_status enqueue_gemm(const void *x, const void *w, void *y, int m, int n, int 
   }
   st = launch_status(sk::launch_gemm(tw, tx, static_cast<uint16_t *>(y), m, n, k, plan.splits,
                                      plan.h, plan.stages, plan.bps, as_stream(stream),
-                                     pdl_enabled(), pfp, warmed ? 0 : -1),
+                                     pdl_enabled(), pfp, warmed ? 0 : -1, x_ready),
                      "gemm");
   if (st == SK_OK && pfp) t_prefetched = hint;
   return st;
@@ -332,6 +332,17 @@ sk_status sk_gemm_bf16(const void *x, const void *w, void *y, int m, int n, int 
   sk::DeviceInfo info;
   if ((st = current_device(&info)) != SK_OK) return st;
   return enqueue_gemm(x, w, y, m, n, k, splits, stream, info);
+}
+
+sk_status sk_gemm_bf16_ex(const void *x, const void *w, void *y, int m, int n, int k, int splits,
+                          unsigned flags, void *stream) {
+  if (flags & ~SK_GEMM_X_READY) return fail(SK_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  sk_status st;
+  if ((st = check_gemm_shape(m, n, k, splits)) != SK_OK) return st;
+  if ((st = check_ptrs16("sk_gemm_bf16_ex(x, w, y)", {x, w, y})) != SK_OK) return st;
+  sk::DeviceInfo info;
+  if ((st = current_device(&info)) != SK_OK) return st;
+  return enqueue_gemm(x, w, y, m, n, k, splits, stream, info, (flags & SK_GEMM_X_READY) != 0);
 }
 
 sk_status sk_gemm_prefetch_next(const void *w_next, int n_next, int k_next) {

@@ -118,10 +118,12 @@ struct GemmPrefetch {
 // (1, splits, 1); tile height h rows, `stages` pipeline stages of `bps` boxes.
 // pf (may be null): the next GEMM's weights to start towards L2. l2_ahead:
 // own weight stages beyond the ring started towards L2 before the dependency
-// wait (-1: about 256 KiB).
+// wait (-1: about 256 KiB). x_ready: the previous kernel does not write x, so
+// its copies do not wait for that kernel (the stores of y still do).
 cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, uint16_t *y, int m,
                         int n, int k, int splits, int h, int stages, int bps, cudaStream_t stream,
-                        bool pdl, const GemmPrefetch *pf = nullptr, int l2_ahead = -1);
+                        bool pdl, const GemmPrefetch *pf = nullptr, int l2_ahead = -1,
+                        bool x_ready = false);
 
 cudaError_t launch_rmsnorm_nvfp4(const uint16_t *y, const uint16_t *norm_w, float eps, float gc,
                                  const float *gs, uint8_t *a, uint8_t *a_sf, uint16_t *z_out,

@@ -44,6 +44,7 @@ struct GemmArgs {
   // index). pf_stages = 0: nothing.
   int pf_stages;
   int pf_h, pf_nkb, pf_bps, pf_tiles, pf_ctas;
+  int x_ready;  // x is not written by the previous kernel: copy it without waiting
 };
 
 // Bounded wait that also gives up as soon as another role raised `abort`.
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // and the next stages towards L2, while the previous kernel finishes
     for (int i = npre; i < nst && i < npre + args.l2_ahead; ++i)
       tma_prefetch_l2_3d(&tmap_w, 0, n0, kb0 + i * B);
-    griddep_wait();
+    if (!args.x_ready) griddep_wait();
     for (int i = 0; i < npre; ++i)
       tma_load_3d(smem_u32(s_x + i * B * kSlotXBytes), &tmap_x, full0 + 8 * i, 0, 0, kb0 + i * B,
                   pol_x);
@@ -250,13 +251,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_sum_accumulators<kNumAcc>(tmem + (static_cast<uint32_t>(warp * 32) << 16),
                                    acc_used(nkb, B, kGemmIssuers), acc);
 
-  // Outputs may still be read by the previous kernel in the stream.
-  griddep_wait();
-
   const int m = args.m, n = args.n;
   uint16_t *y = args.y;
   uint16_t *stage = reinterpret_cast<uint16_t *>(s_w);  // the ring is idle by now
   if (args.splits == 1) {
+    // Outputs may still be read or written by the previous kernel in the stream.
+    griddep_wait();
     store_tile_rows(stage, acc, 0, h, y, n, n0, m, !aborted);
   } else {
     // Split-K across the S ranks of the cluster. Rank r owns tile rows
@@ -331,6 +331,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     __syncthreads();  // the exchange waits are over: *abort_flag is final
     const bool ok = !*abort_flag;
+    // Outputs may still be read or written by the previous kernel in the
+    // stream (the exchange above stays within this cluster's shared memory).
+    griddep_wait();
     if ((R & 7) == 0) {
       store_tile_rows(stage, v, lo, hi > lo ? hi : lo, y, n, n0, m, ok);
     } else if (ok && tid >= lo && tid < hi && n0 + tid < n) {
@@ -744,7 +747,8 @@ int gemm_max_clusters(int device, int splits, int ctas_per_sm) {
 
 cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, uint16_t *y, int m,
                         int n, int k, int splits, int h, int stages, int bps,
-                        cudaStream_t stream, bool pdl, const GemmPrefetch *pf, int l2_ahead) {
+                        cudaStream_t stream, bool pdl, const GemmPrefetch *pf, int l2_ahead,
+                        bool x_ready) {
   if (h % 8 || h < 8 || h > kMmaM || bps < 1 || bps > kMaxBoxesPerStage) return cudaErrorInvalidValue;
   GemmArgs a = {};
   a.y = y;
@@ -767,6 +771,7 @@ cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, ui
     if (a.l2_ahead < 0) a.l2_ahead = 0;
     if (a.l2_ahead > 64) a.l2_ahead = 64;
   }
+  a.x_ready = x_ready ? 1 : 0;
   if (pf && pf->stages > 0) {
     if (pf->h % 8 || pf->h < 8 || pf->h > kMmaM || pf->bps < 1 || pf->bps > kMaxBoxesPerStage ||
         pf->tiles < 1 || pf->splits < 1 || pf->nkb < 1)

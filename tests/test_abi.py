@@ -98,6 +98,15 @@ def test_prefetch_hint_validation(sk):
     assert lib.sk_gemm_prefetch_next(None, 0, 0) == 0
 
 
+def test_gemm_ex_validation(sk):
+    lib = sk.lib()
+    vp = ctypes.c_void_p
+    assert lib.sk_gemm_bf16_ex(vp(P), vp(P), vp(P), 1, 128, 64, 0, 2, None) == 1   # unknown flag
+    assert "flags" in sk.last_error()
+    assert lib.sk_gemm_bf16_ex(vp(P), vp(P), vp(P), 1, 24, 64, 0, 1, None) == 1    # bad n
+    assert lib.sk_gemm_bf16_ex(vp(P + 8), vp(P), vp(P), 1, 128, 64, 0, 1, None) == 1
+
+
 def test_epilogue_validation(sk):
     lib = sk.lib()
     vp = ctypes.c_void_p

@@ -149,6 +149,31 @@ def test_prefetch_hint_leaves_results_unchanged(sk, n2, k2):
     sk.gemm_prefetch_next(None)
 
 
+@pytest.mark.parametrize("m,n,k", [(1, 1024, 4096), (16, 8192, 4096), (5, 400, 1024)])
+def test_x_ready_run_matches_plain_calls(sk, m, n, k):
+    # A run of GEMMs on one input that no kernel writes: with x_ready each call
+    # reads x at once and only its stores wait, so calls overlap. Each result
+    # must equal the plain call's, bit for bit, and a shared output must end
+    # holding the last call's result (stores stay in stream order).
+    x = synth.gemm_x(m, k).to(DEV)
+    ws = [synth.gemm_weight(n, k, 20 + i).to(DEV) for i in range(6)]
+    torch.cuda.synchronize()
+    ref = [sk.gemm_bf16(x, w) for w in ws]
+    outs = [torch.empty(m, n, dtype=torch.bfloat16, device=DEV) for _ in ws]
+    shared = torch.empty(m, n, dtype=torch.bfloat16, device=DEV)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for w, o in zip(ws, outs):
+            sk.gemm_bf16(x, w, out=o, x_ready=True)
+        for w in ws:
+            sk.gemm_bf16(x, w, out=shared, x_ready=True)
+        torch.cuda.synchronize()
+        for r, o in zip(ref, outs):
+            assert torch.equal(o.view(torch.int16), r.view(torch.int16))
+        assert torch.equal(shared.view(torch.int16), ref[-1].view(torch.int16))
+    assert sk.device_status() == 0
+
+
 def test_rows_beyond_m_are_not_written(sk):
     m, n, k = 5, 256, 256
     x = synth.normal_bf16((m, k), 1.0, 30)
