@@ -367,30 +367,42 @@ def run_gpu(args, world, rank, local):
     pin = dict(pin_memory=True)
     h_host = h0.cpu().pin_memory()
     s_host = s0.cpu().pin_memory()
-    out_h = torch.empty(M_ROWS, synth.HIDDEN, dtype=torch.bfloat16, **pin)
-    out_a = torch.empty(M_ROWS, synth.POOLED // 2, dtype=torch.uint8, **pin)
-    out_sf = torch.empty(M_ROWS, synth.POOLED // 16, dtype=torch.uint8, **pin)
+    # two sets of pinned result buffers: step i's results are read on the host
+    # while step i + 1 runs
+    outs = [(torch.empty(M_ROWS, synth.HIDDEN, dtype=torch.bfloat16, **pin),
+             torch.empty(M_ROWS, synth.POOLED // 2, dtype=torch.uint8, **pin),
+             torch.empty(M_ROWS, synth.POOLED // 16, dtype=torch.uint8, **pin)) for _ in range(2)]
     h2d = h_host.numel() * 2 + s_host.numel() * 4
-    d2h = out_h.numel() * 2 + out_a.numel() + out_sf.numel()
+    d2h = sum(t.numel() * t.element_size() for t in outs[0])
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            chain.h[0].copy_(h_host, non_blocking=True)
-            chain.s.copy_(s_host, non_blocking=True)
-            g_chain.replay()
-            out_h.copy_(chain.h[L], non_blocking=True)
-            out_a.copy_(chain.a[L - 1], non_blocking=True)
-            out_sf.copy_(chain.a_sf[L - 1], non_blocking=True)
-        stream.synchronize()
+    def e2e_steps_run(n_steps):
+        """n_steps decode steps as a serving loop runs them: each step copies its
+        inputs in, replays the chain and copies its results out (one stream,
+        so in order); the host queues step i + 1 before it waits for step i's
+        results."""
+        done = None
+        for i in range(n_steps):
+            out_h, out_a, out_sf = outs[i % 2]
+            with torch.cuda.stream(stream):
+                chain.h[0].copy_(h_host, non_blocking=True)
+                chain.s.copy_(s_host, non_blocking=True)
+                g_chain.replay()
+                out_h.copy_(chain.h[L], non_blocking=True)
+                out_a.copy_(chain.a[L - 1], non_blocking=True)
+                out_sf.copy_(chain.a_sf[L - 1], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(stream)
+            if done is not None:
+                done.synchronize()  # step i - 1's results are on the host
+            done = ev
+        done.synchronize()
 
-    for _ in range(3):
-        e2e_step()
+    e2e_steps_run(3)
     e2e_steps = max(10, min(args.steps, 300))
     if dist:
         dist.barrier()
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
+    e2e_steps_run(e2e_steps)
     t_e2e = reduce_max(time.perf_counter() - t0, dist, dev)
     e2e_value = aggregate_rate(bytes_step, e2e_steps, world, t_e2e)
     status = sk.device_status()
