@@ -124,3 +124,27 @@ def test_prefetch_hints_leave_the_chain_unchanged(chain):
     assert torch.equal(c.a, hinted[1]) and torch.equal(c.a_sf, hinted[2])
     assert torch.equal(c.s, hinted[3])
     assert torch.equal(c.u.view(torch.int16), hinted[4].view(torch.int16))
+
+
+@pytest.mark.parametrize("m", [1, 3])
+def test_small_m_chain_matches_oracle(m):
+    # the same chain at a ragged token count (rows past m are zero-filled by the
+    # copy engine and never stored), every layer checked against the oracle on
+    # its GPU inputs, with the next-weight hints on
+    import nvfp4_sm_skinny_gb300 as sk
+    from nvfp4_sm_skinny_gb300.chain import DecodeChain
+
+    c = DecodeChain(layers=3, m=m, device=DEV)
+    assert c.prefetch_next
+    h0 = synth.normal_bf16((m, synth.HIDDEN), 1.0, 7).to(DEV)
+    s0 = synth.normal_f32((m, synth.HIDDEN), 8).to(DEV)
+    c.calibrate(synth.normal_bf16((m, synth.HIDDEN), 1.0, 9).to(DEV), s0)
+    c.set_input(h0, s0)
+    c.s_after = {}
+    for l in range(c.L):
+        s_before = c.s.cpu().numpy().copy()
+        c.layer(l)
+        torch.cuda.synchronize()
+        c.s_after[l] = c.s.cpu().numpy().copy()
+        check_layer(c, l, s_before)
+    assert sk.device_status() == 0
