@@ -38,13 +38,13 @@ struct GemmArgs {
   int bps;           // boxes per stage
   int splits;
   int l2_ahead;      // weight stages started towards L2 before the dependency wait
-  // The GEMM enqueued after this one (tensor map tmap_pf): once this CTA has
-  // issued its last weight copy, it starts towards L2 the first pf_stages
+  // The GEMM enqueued after this one (tensor map tmap_pf): once this CTA's
+  // last weight stage has landed, it starts towards L2 the first pf_stages
   // stages of the next GEMM's CTAs c, c + ctas, ... (c = this CTA's linear
   // index). pf_stages = 0: nothing.
   int pf_stages;
   int pf_h, pf_nkb, pf_bps, pf_tiles, pf_ctas;
-  int x_ready;  // x is not written by the previous kernel: copy it without waiting
+  int x_ready;  // no running kernel writes x: copy it without waiting (the stores of y still wait)
 };
 
 // Bounded wait that also gives up as soon as another role raised `abort`.
