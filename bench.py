@@ -12,10 +12,14 @@ L2, so no flush is needed between steps). The pass is captured once as a CUDA
 graph of the C-ABI calls and replayed; kernels are chained with programmatic
 dependent launch.
 
-Reported: whole-job achieved HBM GB/s (algorithmic bytes / time), the
-dominant kernel's roofline (the skinny GEMM timed alone over the same
-launches), the end-to-end rate with host buffers, the CPU oracle on a bounded
-sample, and the SM clocks sampled during the timed region.
+Reported: whole-job achieved HBM GB/s (algorithmic bytes / time) with the
+spread of the step time, the dominant kernel's roofline (the skinny GEMM timed
+alone over the same launches), the end-to-end rate with host buffers, the
+single-call workloads (`per_config`: the M=1 unpooler shard, the GEMM sweep
+over M and split counts, the pooler + RMSNorm + NVFP4 and the o_proj + dual
+norm, each as µs per call over >= 200 calls with 48 rotated weight copies),
+the CPU oracle on a bounded sample, and the SM clocks sampled during the timed
+region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -286,6 +290,160 @@ def time_graph(graph, steps: int, stream) -> float:
     return e0.elapsed_time(e1) / 1e3
 
 
+def time_graph_steps(graph, steps: int, stream):
+    """(total seconds, per-replay seconds) for `steps` back-to-back replays:
+    one CUDA event between consecutive replays on the replay stream."""
+    import torch
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(steps):
+            graph.replay()
+            ev[i + 1].record(stream)
+    ev[-1].synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(steps)]
+    return ev[0].elapsed_time(ev[-1]) / 1e3, per
+
+
+def quantiles(xs, qs=(0.1, 0.5, 0.9)):
+    """Linear-interpolated quantiles of a non-empty list."""
+    v = sorted(xs)
+    out = []
+    for q in qs:
+        pos = q * (len(v) - 1)
+        lo = int(pos)
+        hi = min(lo + 1, len(v) - 1)
+        out.append(v[lo] + (v[hi] - v[lo]) * (pos - lo))
+    return out
+
+
+def single_call_workloads(sk, synth, dev, stream, peak, min_calls: int = 200, copies: int = 48):
+    """Per-call timings of the single-call workloads, each point a CUDA graph of
+    one call per weight copy (48 copies, more bytes than L2), replayed until at
+    least `min_calls` calls are timed: µs per call as median, p10 and p90 over
+    the replays, algorithmic GB/s and % of the HBM peak at the median.
+
+    * the unpooler shard M=1 [1024,4096] and the GEMM sweep M in {1,2,4,8,16} x
+      (N,K) in {(1024,4096),(8192,4096)} at the automatic split, plus every
+      split count S in {1,2,4,8} at M=16;
+    * the pooler GEMM [4096,8192] + RMSNorm + NVFP4 at b in {1,8,16};
+    * the o_proj GEMM [8192,1024] + dual norm at b in {1,4,16}.
+    Automatic-split points also report `hinted_us_p50`: the same calls, each
+    told the next call's weight (sk_gemm_prefetch_next)."""
+    import torch
+
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    out = {}
+
+    def timed(calls):
+        with torch.cuda.stream(stream):
+            for c in calls:
+                c()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for c in calls:
+                c()
+        for _ in range(3):
+            with torch.cuda.stream(stream):
+                g.replay()
+        reps = max(5, -(-min_calls // len(calls)))
+        _, per = time_graph_steps(g, reps, stream)
+        del g
+        return [t / len(calls) for t in per], reps * len(calls)
+
+    def hinted(ws, call):
+        def one(i):
+            def f():
+                sk.gemm_prefetch_next(ws[(i + 1) % len(ws)])
+                call(ws[i])
+            return f
+        return [one(i) for i in range(len(ws))]
+
+    def put(key, workload, m, n, k, splits, nbytes, per, ncalls, hint_per=None):
+        p10, p50, p90 = quantiles(per)
+        gbs = nbytes / p50 / 1e9
+        r = {"workload": workload, "m": m, "n": n, "k": k, "splits": splits,
+             "us_p50": round(p50 * 1e6, 3), "us_p10": round(p10 * 1e6, 3),
+             "us_p90": round(p90 * 1e6, 3), "calls": ncalls, "bytes": nbytes,
+             "gbs": round(gbs, 1), "pct_of_peak": round(100.0 * gbs / peak, 2)}
+        if hint_per is not None:
+            h50 = quantiles(hint_per, (0.5,))[0]
+            r["hinted_us_p50"] = round(h50 * 1e6, 3)
+            r["hinted_pct_of_peak"] = round(100.0 * nbytes / h50 / 1e9 / peak, 2)
+        out[key] = r
+
+    for n, k in ((1024, 4096), (8192, 4096)):
+        ws = [synth.gemm_weight(n, k, i, device=dev) for i in range(copies)]
+        for m in (1, 2, 4, 8, 16):
+            x = synth.gemm_x(m, k).to(dev)
+            y = torch.empty(m, n, **bf)
+            nbytes = 2 * n * k + 2 * m * k + 2 * m * n
+            per, nc = timed([lambda w=w: sk.gemm_bf16(x, w, out=y, stream=stream) for w in ws])
+            hper, _ = timed(hinted(ws, lambda w: sk.gemm_bf16(x, w, out=y, stream=stream)))
+            wl = "unpooler GEMM" if m == 1 and n == 1024 else "GEMM"
+            put(f"gemm_m{m}_n{n}_k{k}", wl, m, n, k, f"auto({sk.gemm_splits(m, n, k)})", nbytes,
+                per, nc, hper)
+            if m == 16:
+                for S in (1, 2, 4, 8):
+                    if sk.gemm_supported(m, n, k, S) is not None:
+                        continue
+                    per, nc = timed([lambda w=w, S=S: sk.gemm_bf16(x, w, out=y, splits=S,
+                                                                  stream=stream) for w in ws])
+                    put(f"gemm_m{m}_n{n}_k{k}_s{S}", "GEMM", m, n, k, S, nbytes, per, nc)
+        sk.gemm_prefetch_next(None)
+        del ws
+        torch.cuda.empty_cache()
+
+    H, P = synth.HIDDEN, synth.POOLED
+    ws = [synth.normal_bf16((P, H), 0.02, 200 + i, device=dev) for i in range(copies)]
+    nw = synth.normal_bf16((P,), 0.1, 300, device=dev)
+    gs = torch.tensor([300.0], dtype=torch.float32, device=dev)
+    for b in (1, 8, 16):
+        x = synth.normal_bf16((b, H), 1.0, 0, device=dev)
+        a = torch.empty(b, P // 2, dtype=torch.uint8, device=dev)
+        a_sf = torch.empty(b, P // 16, dtype=torch.uint8, device=dev)
+        wsp = torch.empty(sk.gemm_rmsnorm_nvfp4_workspace(b, P), dtype=torch.uint8, device=dev)
+
+        def call(w, x=x, a=a, a_sf=a_sf, wsp=wsp):
+            sk.gemm_rmsnorm_nvfp4(x, w, nw, synth.EPS, synth.GAIN_CENTER, gs, a=a, a_sf=a_sf,
+                                  workspace=wsp, stream=stream)
+        per, nc = timed([lambda w=w: call(w) for w in ws])
+        hper, _ = timed(hinted(ws, call))
+        put(f"pooler_nvfp4_b{b}", "pooler GEMM + RMSNorm + NVFP4", b, P, H,
+            f"auto({sk.gemm_splits(b, P, H)})",
+            2 * P * H + 2 * b * H + 2 * P + 4 + b * P // 2 + b * P // 16, per, nc, hper)
+    sk.gemm_prefetch_next(None)
+    del ws
+    torch.cuda.empty_cache()
+
+    K = synth.OPROJ_K
+    ws = [synth.normal_bf16((H, K), 0.02, 400 + i, device=dev) for i in range(copies)]
+    post_w = synth.normal_bf16((H,), 0.1, 500, mean=1.0, device=dev)
+    pre_w = synth.normal_bf16((H,), 0.1, 501, mean=1.0, device=dev)
+    beta = synth.uniform_bf16((H,), 0.5, 1.5, 502, device=dev)
+    for b in (1, 4, 16):
+        x = synth.normal_bf16((b, K), 1.0, 0, device=dev)
+        # the residual stream is updated in place and drifts from call to call
+        s_res = synth.normal_f32((b, H), 503, device=dev)
+        o = torch.empty(b, H, **bf)
+        wsp = torch.empty(sk.gemm_dual_norm_workspace(b, H), dtype=torch.uint8, device=dev)
+
+        def call(w, x=x, s_res=s_res, o=o, wsp=wsp):
+            sk.gemm_dual_norm(x, w, s_res, post_w, 1.0, beta, pre_w, out=o, eps_post=synth.EPS,
+                              eps_pre=synth.EPS, workspace=wsp, stream=stream)
+        per, nc = timed([lambda w=w: call(w) for w in ws])
+        hper, _ = timed(hinted(ws, call))
+        put(f"oproj_dual_b{b}", "o_proj GEMM + dual norm", b, H, K,
+            f"auto({sk.gemm_splits(b, H, K)})",
+            2 * H * K + 2 * b * K + 3 * 2 * H + 2 * 4 * b * H + 2 * b * H, per, nc, hper)
+    sk.gemm_prefetch_next(None)
+    del ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args, world, rank, local):
     import torch
 
@@ -325,7 +483,7 @@ def run_gpu(args, world, rank, local):
     if rank == 0:
         sampler.start()
         time.sleep(0.25)
-    t_chain = time_graph(g_chain, args.steps, stream)
+    t_chain, step_s = time_graph_steps(g_chain, args.steps, stream)
     clocks = sampler.stop() if rank == 0 else None
     torch.cuda.synchronize(dev)
     if dist:
@@ -407,6 +565,11 @@ def run_gpu(args, world, rank, local):
     e2e_value = aggregate_rate(bytes_step, e2e_steps, world, t_e2e)
     status = sk.device_status()
 
+    per_config = None
+    if rank == 0 and not args.no_per_config:
+        per_config = single_call_workloads(sk, synth, dev, stream, peak)
+        status |= sk.device_status()
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_seconds)
@@ -432,8 +595,11 @@ def run_gpu(args, world, rank, local):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "bytes_per_step": bytes_step},
             "pct_of_peak": round(100.0 * value / world / peak, 2),
+            "step_ms": dict(zip(("p10", "p50", "p90"),
+                                (round(q * 1e3, 4) for q in quantiles(step_s)))),
             "peak_hbm_gbs": {"value": peak, "source": peak_src},
             "per_op": per_op,
+            "per_config": per_config,
             "roofline": {"bound": "hbm", "kernel": "sk::gemm_kernel (all chain GEMM launches)",
                          "achieved": round(achieved, 2), "peak": peak,
                          "peak_source": f"{peak_src} HBM copy bandwidth", "unit": "GB/s",
@@ -596,6 +762,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["sk", "reference"], default="sk")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the single-call workloads (per_config) after the chain")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="chain depth (48 is the benchmark; fewer only for small profiling runs)")

@@ -60,8 +60,8 @@ typedef enum sk_status {
 #define SK_DEVICE_WAIT_PRODUCER 0x1u /* weight/activation copy never landed */
 #define SK_DEVICE_WAIT_MMA 0x2u      /* tensor-core stage never filled      */
 #define SK_DEVICE_WAIT_EPILOGUE 0x4u /* accumulator never completed         */
-#define SK_DEVICE_WAIT_GRID 0x8u     /* a grid-wide barrier never completed  */
 #define SK_DEVICE_WAIT_PROBE 0x10u   /* sk_wait_probe's wait ran out (expected) */
+#define SK_DEVICE_WAIT_TEARDOWN 0x20u /* after an abort, the MMAs never quiesced before TMEM release */
 
 /* Message of the last failed call on this host thread ("" if none). The
    string lives in thread-local storage owned by the library. */
@@ -248,46 +248,6 @@ sk_status sk_gemm_dual_norm(const void *x, const void *w, float *resid, const vo
                             void *workspace, size_t workspace_bytes, int m, int n, int k,
                             int splits, void *stream);
 
-/* Size in bytes of the workspace sk_decode_layer needs (grid barrier words and
-   per-CTA partial sums; independent of the shapes). */
-size_t sk_decode_layer_workspace(void);
-
-/*
- * sk_decode_layer -- one decode layer of the hot path in a single persistent
- * kernel (the chain of cutedsl/oproj/batt OProjection.run and
- * AttentionBoundary.run, cutedsl/moe/pooler_gather Pooler.run for an NVFP4
- * layer, and cutedsl/gemm/unpooler Unpooler.run, on one GPU):
- *   partial = h_in @ w_o^T                                  [m, hidden]  (BF16-rounded)
- *   resid, u = dual norm of partial (as sk_dual_norm_residual)            [m, hidden]
- *   y       = u @ w_p^T                                     [m, pooled]  (BF16-rounded)
- *   a, a_sf, z = pre-expert RMSNorm + NVFP4 of y (as sk_rmsnorm_nvfp4)    [m, pooled]
- *   h_out   = z @ w_u^T                                     [m, hidden]
- * Same arithmetic per element as the separate calls (the partial sums are
- * taken in a different fixed order, so results match them within the
- * library's tolerances, and are bitwise reproducible run to run).
- *   h_in BF16 [m, k_oproj]; w_o BF16 [hidden, k_oproj]; w_p BF16 [pooled, hidden];
- *   w_u BF16 [hidden, pooled]; resid FP32 [m, hidden] (read and written);
- *   post_w BF16 [hidden] or NULL; beta, pre_w BF16 [hidden]; norm_w BF16 [pooled];
- *   global_scale device FP32 [1]; outputs u_out BF16 [m, hidden], z_out BF16
- *   [m, pooled], a u8 [m, pooled/2], a_sf u8 [m, pooled/16], h_out BF16 [m, hidden];
- *   optional outputs (NULL = not stored): partial_out BF16 [m, hidden] (the
- *   o_proj partial) and y_out BF16 [m, pooled] (the pooler rows before the norm).
- *   workspace: >= sk_decode_layer_workspace() bytes, 256-byte aligned; the call
- *   clears its first 256 bytes on `stream` before the kernel.
- *   1 <= m <= 16; hidden, pooled, k_oproj multiples of 64; hidden and pooled at
- *   most 128 x (number of SMs). Needs every CTA of the grid resident at once
- *   (cooperative launch, one CTA per SM); returns SK_ERR_UNSUPPORTED if the
- *   device cannot host it.
- */
-sk_status sk_decode_layer(const void *h_in, const void *w_o, const void *w_p, const void *w_u,
-                          float *resid, const void *post_w, float alpha, const void *beta,
-                          const void *pre_w, const void *norm_w, const float *global_scale,
-                          void *u_out, void *z_out, uint8_t *a, uint8_t *a_sf, void *h_out,
-                          void *partial_out, void *y_out, float eps_post, float eps_pre,
-                          float gc_post, float gc_pre, float eps_pool, float gc_pool,
-                          void *workspace, size_t workspace_bytes, int m, int hidden, int pooled,
-                          int k_oproj, void *stream);
-
 /* Bytes of the static device scratch behind sk_gemm_rmsnorm_nvfp4_static:
    room for a BF16 [m, n] GEMM output with m * n <= 131072 (16 x 8192). */
 #define SK_STATIC_SCRATCH_BYTES (16u * 8192u * 2u)
@@ -306,11 +266,14 @@ sk_status sk_decode_layer(const void *h_in, const void *w_o, const void *w_p, co
  *   per device that loads the library, held until the process exits). The
  *   call allocates nothing.
  *   The first call on a device looks up that array's device address (once per
- *   device, with the device current); make that first call before any stream
- *   capture. Every call shares the array and it keeps the last call's
- *   contents; it needs no clearing, since the GEMM rewrites what the norm then
- *   reads. Calls that may run at the same time on the GPU (unordered streams)
- *   race on the array and give wrong results.
+ *   device and CUDA context, with the device current); make that first call
+ *   before any stream capture. A device reset destroys the context that holds
+ *   the array: the next call looks the address up again, so after a reset the
+ *   first call, too, should come before any capture. Every call shares the
+ *   array and it keeps the last call's contents; it needs no clearing, since
+ *   the GEMM rewrites what the norm then reads. Calls that may run at the same
+ *   time on the GPU (unordered streams) race on the array and give wrong
+ *   results.
  */
 sk_status sk_gemm_rmsnorm_nvfp4_static(const void *x, const void *w, const void *norm_w,
                                        float eps, float gain_center, const float *global_scale,

@@ -78,9 +78,6 @@ def lib() -> ctypes.CDLL:
             "sk_gemm_dual_norm_workspace": ([i, i], sz),
             "sk_gemm_dual_norm": ([vp, vp, vp, vp, f, vp, vp, vp, f, f, f, f, vp, sz, i, i, i, i, vp], i),
             "sk_gemm_rmsnorm_nvfp4_static": ([vp, vp, vp, f, f, vp, vp, vp, vp, i, i, i, i, vp], i),
-            "sk_decode_layer_workspace": ([], sz),
-            "sk_decode_layer": ([vp, vp, vp, vp, vp, vp, f, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                 vp, f, f, f, f, f, f, vp, sz, i, i, i, i, vp], i),
             "sk_device_status": ([ctypes.POINTER(ctypes.c_uint32), i], i),
             "sk_convert_probe": ([i, vp, vp, i, vp], i),
             "sk_wait_probe": ([ctypes.c_uint, vp], i),
@@ -357,49 +354,6 @@ def gemm_dual_norm(x, w, resid, post_w, alpha: float, beta, pre_w, out=None,
         eps_post, eps_pre, gc_post, gc_pre, _ptr(workspace),
         workspace.numel() * workspace.element_size(), m, n, k, splits, _stream(stream)))
     return out, workspace
-
-
-# ---------------------------------------------------- fused decode layer ----
-def decode_layer_workspace() -> int:
-    return int(lib().sk_decode_layer_workspace())
-
-
-def decode_layer(h_in, w_o, w_p, w_u, resid, post_w, alpha: float, beta, pre_w, norm_w,
-                 global_scale, u_out, z_out, a, a_sf, h_out, workspace, partial_out=None,
-                 y_out=None, eps_post: float = 1e-6, eps_pre: float = 1e-6, gc_post: float = 0.0,
-                 gc_pre: float = 0.0, eps_pool: float = 1e-6, gc_pool: float = 1.0, stream=None):
-    """One decode layer in one persistent kernel: o_proj, dual norm, pooler +
-    RMSNorm + NVFP4, unpooler. Every output buffer is the caller's."""
-    m, ko = h_in.shape
-    hidden = w_o.shape[0]
-    pooled = w_p.shape[0]
-    _need(h_in, torch.bfloat16, (m, ko), "h_in")
-    _need(w_o, torch.bfloat16, (hidden, ko), "w_o")
-    _need(w_p, torch.bfloat16, (pooled, hidden), "w_p")
-    _need(w_u, torch.bfloat16, (hidden, pooled), "w_u")
-    _need(resid, torch.float32, (m, hidden), "resid")
-    if post_w is not None:
-        _need(post_w, torch.bfloat16, (hidden,), "post_w")
-    _need(beta, torch.bfloat16, (hidden,), "beta")
-    _need(pre_w, torch.bfloat16, (hidden,), "pre_w")
-    _need(norm_w, torch.bfloat16, (pooled,), "norm_w")
-    _need(global_scale, torch.float32, (1,), "global_scale")
-    _need(u_out, torch.bfloat16, (m, hidden), "u_out")
-    _need(z_out, torch.bfloat16, (m, pooled), "z_out")
-    _need(a, torch.uint8, (m, pooled // 2), "a")
-    _need(a_sf, torch.uint8, (m, pooled // 16), "a_sf")
-    _need(h_out, torch.bfloat16, (m, hidden), "h_out")
-    if partial_out is not None:
-        _need(partial_out, torch.bfloat16, (m, hidden), "partial_out")
-    if y_out is not None:
-        _need(y_out, torch.bfloat16, (m, pooled), "y_out")
-    _check(lib().sk_decode_layer(
-        _ptr(h_in), _ptr(w_o), _ptr(w_p), _ptr(w_u), _ptr(resid), _ptr(post_w), alpha, _ptr(beta),
-        _ptr(pre_w), _ptr(norm_w), _ptr(global_scale), _ptr(u_out), _ptr(z_out), _ptr(a),
-        _ptr(a_sf), _ptr(h_out), _ptr(partial_out), _ptr(y_out), eps_post, eps_pre, gc_post,
-        gc_pre, eps_pool, gc_pool, _ptr(workspace), workspace.numel() * workspace.element_size(),
-        m, hidden, pooled, ko, _stream(stream)))
-    return h_out
 
 
 # ----------------------------------------------------------- diagnostics ----

@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsk.so")
 
 SOURCES = ["sk_api.cu", "sk_kernels.cu", "sk_static_scratch.cu"]
-HEADERS = ["sk_internal.h", "sk_ptx.cuh", "sk_decode.cuh"]
+HEADERS = ["sk_internal.h", "sk_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -75,16 +75,6 @@ class DecodeChain:
         self.ws_o = torch.zeros(layers, sk.gemm_dual_norm_workspace(m, H), dtype=torch.uint8, device=dev)
         self.ws_p = torch.zeros(layers, sk.gemm_rmsnorm_nvfp4_workspace(m, P), dtype=torch.uint8,
                                 device=dev)
-        self.ws_dec = torch.zeros(sk.decode_layer_workspace(), dtype=torch.uint8, device=dev)
-        self.p_dbg = None  # optional per-layer o_proj partials / pooler rows (fused path)
-        self.y_dbg = None
-
-    def keep_intermediates(self) -> None:
-        """Have the fused path also store each layer's o_proj partial and the
-        pooler rows before the norm (for parity checks)."""
-        dev = self.device
-        self.p_dbg = torch.zeros(self.L, self.m, H, dtype=torch.bfloat16, device=dev)
-        self.y_dbg = torch.zeros(self.L, self.m, P, dtype=torch.bfloat16, device=dev)
 
     def set_input(self, h0: torch.Tensor, s0: torch.Tensor) -> None:
         self.h[0].copy_(h0)
@@ -123,20 +113,6 @@ class DecodeChain:
     def forward(self, stream=None) -> None:
         for l in range(self.L):
             self.layer(l, stream)
-
-    def layer_fused(self, l: int, stream=None) -> None:
-        """Layer l as one persistent kernel (sk_decode_layer)."""
-        sk.decode_layer(self.h[l], self.w_o[l], self.w_p[l], self.w_u[l], self.s, self.post_w[l],
-                        self.alpha, self.beta[l], self.pre_w[l], self.norm_w[l], self.gs[l],
-                        self.u[l], self.z[l], self.a[l], self.a_sf[l], self.h[l + 1], self.ws_dec,
-                        partial_out=None if self.p_dbg is None else self.p_dbg[l],
-                        y_out=None if self.y_dbg is None else self.y_dbg[l],
-                        eps_post=self.eps, eps_pre=self.eps, eps_pool=self.eps, gc_pool=self.gc,
-                        stream=stream)
-
-    def forward_fused(self, stream=None) -> None:
-        for l in range(self.L):
-            self.layer_fused(l, stream)
 
     def gemms_only(self, stream=None) -> None:
         """The chain's three GEMMs per layer without their epilogues (same
@@ -180,4 +156,3 @@ class DecodeChain:
 
     launches_per_layer = 5
     gemm_launches_per_layer = 3
-    fused_launches_per_layer = 1

@@ -7,7 +7,6 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
-#include <numeric>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -530,115 +529,6 @@ sk_status sk_gemm_dual_norm(const void *x, const void *w, float *resid, const vo
                            static_cast<uint16_t *>(out), eps_post, eps_pre, gc_post, gc_pre, m, n,
                            as_stream(stream), pdl_enabled()),
       "dual_norm");
-}
-
-size_t sk_decode_layer_workspace(void) { return 256 + 3 * 1024 * 16 * sizeof(float); }
-
-sk_status sk_decode_layer(const void *h_in, const void *w_o, const void *w_p, const void *w_u,
-                          float *resid, const void *post_w, float alpha, const void *beta,
-                          const void *pre_w, const void *norm_w, const float *global_scale,
-                          void *u_out, void *z_out, uint8_t *a, uint8_t *a_sf, void *h_out,
-                          void *partial_out, void *y_out, float eps_post, float eps_pre,
-                          float gc_post, float gc_pre, float eps_pool, float gc_pool,
-                          void *workspace, size_t workspace_bytes, int m, int hidden, int pooled,
-                          int k_oproj, void *stream) {
-  if (m < 1 || m > SK_MAX_M)
-    return fail(SK_ERR_INVALID_ARG, "m=%d: needs 1 <= m <= %d token rows", m, SK_MAX_M);
-  if (hidden <= 0 || hidden % sk::kBlockK || pooled <= 0 || pooled % sk::kBlockK || k_oproj <= 0 ||
-      k_oproj % sk::kBlockK)
-    return fail(SK_ERR_INVALID_ARG, "hidden=%d, pooled=%d, k_oproj=%d: need positive multiples of %d",
-                hidden, pooled, k_oproj, sk::kBlockK);
-  sk_status st = check_ptrs16("sk_decode_layer(h_in, w_o, w_p, w_u, resid, beta, pre_w, norm_w, "
-                              "u_out, z_out, a, h_out, workspace)",
-                              {h_in, w_o, w_p, w_u, resid, beta, pre_w, norm_w, u_out, z_out, a,
-                               h_out, workspace});
-  if (st != SK_OK) return st;
-  if (post_w && !aligned16(post_w)) return fail(SK_ERR_INVALID_ARG, "post_w is not 16-byte aligned");
-  if ((partial_out && !aligned16(partial_out)) || (y_out && !aligned16(y_out)))
-    return fail(SK_ERR_INVALID_ARG, "partial_out / y_out not 16-byte aligned");
-  if (!a_sf) return fail(SK_ERR_INVALID_ARG, "a_sf is null");
-  if (!global_scale || (reinterpret_cast<uintptr_t>(global_scale) & 3))
-    return fail(SK_ERR_INVALID_ARG, "global_scale must be a 4-byte aligned device FP32 [1]");
-  if (workspace_bytes < sk_decode_layer_workspace())
-    return fail(SK_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes,
-                sk_decode_layer_workspace());
-  sk::DeviceInfo info;
-  int dev = 0;
-  if ((st = sk::checked_device(&info, &dev)) != SK_OK) return st;
-  const int G = info.sm_count;
-  if (G > 1024) return fail(SK_ERR_UNSUPPORTED, "more than 1024 SMs");
-  // one tile per CTA and phase; the pooler's tiles are whole NVFP4 blocks
-  sk::DecodeArgs args = {};
-  args.m = m;
-  args.H = hidden;
-  args.P = pooled;
-  args.Ko = k_oproj;
-  const int rows[3] = {hidden, pooled, hidden};
-  const int ks[3] = {k_oproj, hidden, pooled};
-  int slot_w = 0;
-  for (int p = 0; p < 3; ++p) {
-    // whole 8-row swizzle atoms; the pooler's tiles hold whole NVFP4 blocks
-    int h = (rows[p] + G - 1) / G;
-    h = p == 1 ? (h + 15) / 16 * 16 : (h + 7) / 8 * 8;
-    if (h > sk::kMmaM)
-      return fail(SK_ERR_UNSUPPORTED, "%d rows need more than %d rows per CTA on %d SMs", rows[p],
-                  sk::kMmaM, G);
-    args.h[p] = h;
-    args.tiles[p] = (rows[p] + h - 1) / h;
-    args.nkb[p] = ks[p] / sk::kBlockK;
-    const int sw = ((h + 7) / 8) * 1024;
-    if (sw > slot_w) slot_w = sw;
-  }
-  args.slot_w = slot_w;
-  const size_t cap = info.max_smem_optin - 1024;
-  // a stage size that divides every phase's K blocks
-  const int nkb_all = std::gcd(args.nkb[0], std::gcd(args.nkb[1], args.nkb[2]));
-  choose_ring(nkb_all, cap, [&](int s, int b) { return sk::decode_smem_bytes(slot_w, s, b); },
-              &args.stages, &args.bps);
-  // the ring serves every phase in turn: keep all of its stages
-  while (args.stages < sk::kMaxStages &&
-         sk::decode_smem_bytes(slot_w, args.stages + 1, args.bps) <= cap)
-    ++args.stages;
-  const size_t smem = sk::decode_smem_bytes(slot_w, args.stages, args.bps);
-  if (sk::decode_blocks_per_sm(smem) < 1)
-    return fail(SK_ERR_UNSUPPORTED, "the fused layer kernel cannot be resident with %zu bytes", smem);
-  args.post_w = static_cast<const uint16_t *>(post_w);
-  args.beta = static_cast<const uint16_t *>(beta);
-  args.pre_w = static_cast<const uint16_t *>(pre_w);
-  args.norm_w = static_cast<const uint16_t *>(norm_w);
-  args.alpha = alpha;
-  args.eps_post = eps_post;
-  args.eps_pre = eps_pre;
-  args.gc_post = gc_post;
-  args.gc_pre = gc_pre;
-  args.eps_pool = eps_pool;
-  args.gc_pool = gc_pool;
-  args.gs = global_scale;
-  args.s = resid;
-  args.u = static_cast<uint16_t *>(u_out);
-  args.z = static_cast<uint16_t *>(z_out);
-  args.h_out = static_cast<uint16_t *>(h_out);
-  args.a = a;
-  args.a_sf = a_sf;
-  args.p_out = static_cast<uint16_t *>(partial_out);
-  args.y_out = static_cast<uint16_t *>(y_out);
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
-  args.bar = reinterpret_cast<unsigned *>(ws);
-  args.gabort = reinterpret_cast<unsigned *>(ws + 128);  // its own cache line
-  args.part = reinterpret_cast<float *>(ws + 256);
-
-  sk::DecodeMaps maps;
-  const void *wts[3] = {w_o, w_p, w_u};
-  const void *xs[3] = {h_in, u_out, z_out};
-  const int xcols[3] = {k_oproj, hidden, pooled};
-  for (int p = 0; p < 3; ++p) {
-    if ((st = make_map(&maps.w[p], wts[p], rows[p], ks[p], args.h[p], args.bps)) != SK_OK) return st;
-    if ((st = make_map(&maps.x[p], xs[p], m, xcols[p], sk::kTokTile, args.bps)) != SK_OK) return st;
-  }
-  cudaError_t e = cudaMemsetAsync(workspace, 0, 256, as_stream(stream));
-  if (e != cudaSuccess) return fail(SK_ERR_CUDA, "workspace clear failed: %s", cudaGetErrorString(e));
-  return launch_status(sk::launch_decode_layer(maps, args, G, smem, as_stream(stream), false),
-                       "decode_layer");
 }
 
 sk_status sk_wait_probe(unsigned limit_us, void *stream) {

@@ -143,66 +143,6 @@ cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t stream);
 
 cudaError_t read_device_status(uint32_t *out, bool clear);
 
-// Fused decode layer (sk_decode.cuh): arguments, layout, launch.
-// Warp 0: TMA producer; warps 1..kDecIssuers: MMA issuers (tile rows are
-// fewer than 128 here, so each instruction carries less weight and more
-// issuers are needed); the last four warps: epilogue, one per TMEM lane
-// quadrant.
-constexpr int kDecIssuers = 4;
-constexpr int kDecThreads = 32 * (1 + kDecIssuers + 4);
-constexpr int kDecNumAcc = kDecIssuers;              // one accumulator per issuer
-constexpr int kDecTmemCols = kDecNumAcc * kTokTile;  // 64
-constexpr int kDecPhases = 3;  // 0: o_proj, 1: pooler, 2: unpooler
-
-struct DecodeMaps {
-  CUtensorMap w[kDecPhases];  // weights, boxes of h[p] rows x 64 columns
-  CUtensorMap x[kDecPhases];  // activations h_in, u, z: boxes of 16 rows x 64 columns
-};
-
-struct DecodeArgs {
-  int m, H, P, Ko;
-  int h[kDecPhases];      // tile rows per phase
-  int tiles[kDecPhases];  // CTA c owns tile c of phase p when c < tiles[p]
-  int nkb[kDecPhases];    // 64-wide K blocks per phase
-  int stages, bps;        // pipeline stages, boxes per stage
-  int slot_w;             // bytes per weight slot
-  const uint16_t *post_w, *beta, *pre_w, *norm_w;
-  float alpha, eps_post, eps_pre, gc_post, gc_pre, eps_pool, gc_pool;
-  const float *gs;
-  float *s;                       // residual stream [m, H], updated in place
-  uint16_t *u, *z, *h_out;        // [m, H], [m, P], [m, H]
-  uint16_t *p_out, *y_out;        // optional: o_proj partial [m, H], pooler rows [m, P]
-  uint8_t *a, *a_sf;              // [m, P/2], [m, P/16]
-  unsigned *bar;                  // workspace: grid barrier counter (0 at launch)
-  unsigned *gabort;               // workspace: abort flag (0 at launch)
-  float *part;                    // workspace: [3][gridDim.x][16] partial sums
-};
-
-struct DecodeLayout {
-  int x_off, bar_off, red_off, total;
-};
-
-__host__ __device__ inline DecodeLayout decode_layout(int slot_w, int stages, int bps) {
-  DecodeLayout L;
-  const int nslot = stages * bps;
-  L.x_off = nslot * slot_w;
-  int end = L.x_off + nslot * kSlotXBytes;
-  const int mma_end = (nslot - 1) * slot_w + kMmaABytes;
-  if (mma_end > end) end = mma_end;
-  L.bar_off = (end + 7) / 8 * 8;
-  // full[stages], empty[stages], done[3], then TMEM address and a flag
-  L.red_off = L.bar_off + (2 * stages + kDecPhases) * 8 + 16;
-  // epilogue scratch: red[4][16] + tot[16] floats
-  L.total = L.red_off + (4 * 16 + 16) * 4;
-  return L;
-}
-
-cudaError_t launch_decode_layer(const DecodeMaps &maps, const DecodeArgs &args, int grid,
-                                size_t smem, cudaStream_t stream, bool pdl);
-size_t decode_smem_bytes(int slot_w, int stages, int bps);
-// CTAs of decode_layer_kernel that fit one SM with `smem` bytes.
-int decode_blocks_per_sm(size_t smem);
-
 // The current device, checked to be compute capability 10.3, set up.
 sk_status checked_device(DeviceInfo *info, int *device);
 bool pdl_on();

@@ -246,8 +246,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const bool aborted = *abort_flag != 0;
   tc_fence_after_sync();
 
+  // After an abort the accumulators may still be written by MMAs in flight:
+  // they are not read, and nothing is stored.
   float acc[kTokTile];
-  if (warp < 4)
+#pragma unroll
+  for (int t = 0; t < kTokTile; ++t) acc[t] = 0.0f;
+  if (warp < 4 && !aborted)
     tmem_sum_accumulators<kNumAcc>(tmem + (static_cast<uint32_t>(warp * 32) << 16),
                                    acc_used(nkb, B, kGemmIssuers), acc);
 
@@ -345,7 +349,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 2) {
+    // The MMAs' final commit may not have arrived if the first wait ran out:
+    // wait for it once more (bounded) before the columns are released.
+    if (aborted && lane == 0 && !mbar_wait_idle(done_bar, 0, kWaitLimitNs))
+      atomicOr(&g_device_status, SK_DEVICE_WAIT_TEARDOWN);
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 // ----------------------------------------------------------------------------
@@ -637,12 +649,6 @@ __global__ void convert_probe_kernel(int kind, const void *__restrict__ in, void
   }
 }
 
-}  // namespace sk
-
-#include "sk_decode.cuh"
-
-namespace sk {
-
 // ---------------------------------------------------------------- host side
 size_t gemm_smem_bytes(int h, int stages, int bps, int splits) {
   return 1024 + static_cast<size_t>(gemm_layout(h, stages, bps, splits).total);
@@ -703,10 +709,6 @@ cudaError_t device_setup(int device, DeviceInfo *info) {
                                     static_cast<int>(d.max_smem_optin - fa.sharedSizeBytes))))
         return e;
       if ((e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)))
-        return e;
-      if ((e = cudaFuncGetAttributes(&fa, decode_layer_kernel))) return e;
-      if ((e = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(d.max_smem_optin - fa.sharedSizeBytes))))
         return e;
     }
     g_info[device] = d;
@@ -842,12 +844,3 @@ cudaError_t read_device_status(uint32_t *out, bool clear) {
 
 }  // namespace sk
 
-namespace sk {
-int decode_blocks_per_sm(size_t smem) {
-  int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, decode_layer_kernel, kDecThreads, smem) !=
-      cudaSuccess)
-    return 0;
-  return nb;
-}
-}  // namespace sk

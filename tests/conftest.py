@@ -32,6 +32,25 @@ def pytest_collection_modifyitems(config, items):
             item.add_marker(skip)
 
 
+def pytest_terminal_summary(terminalreporter):
+    # Strict-form GEMM parity: per labelled case, how many outputs lay more
+    # than one BF16 ulp from the oracle's correctly rounded result (accepted
+    # only through the cancellation bound).
+    try:
+        from parity import GEMM_RECORDS
+    except ImportError:  # pragma: no cover
+        return
+    if not GEMM_RECORDS:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", "GEMM outputs beyond 1 BF16 ulp of the oracle (strict form)")
+    total = sum(r[1] for r in GEMM_RECORDS)
+    outs = sum(r[2] for r in GEMM_RECORDS)
+    for label, n_ii, n, dmax in GEMM_RECORDS:
+        tr.write_line(f"{label}: {n_ii} of {n} beyond 1 ulp (max distance {dmax} ulp)")
+    tr.write_line(f"all cases: {total} of {outs} outputs beyond 1 ulp ({total / max(outs, 1):.2e})")
+
+
 def read_cases(name):
     """Parse a golden fixture: ``key: values`` lines, cases split by blank lines."""
     cases, cur = [], {}

@@ -84,3 +84,11 @@ def test_warmup_floor():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "1"],
                        capture_output=True, text=True, timeout=60)
     assert r.returncode != 0
+
+
+def test_quantiles_interpolate():
+    import bench
+
+    assert bench.quantiles([3.0, 1.0, 2.0], (0.0, 0.5, 1.0)) == [1.0, 2.0, 3.0]
+    assert bench.quantiles([0.0, 10.0], (0.1, 0.9)) == pytest.approx([1.0, 9.0])
+    assert bench.quantiles([5.0]) == [5.0, 5.0, 5.0]

@@ -37,7 +37,8 @@ def check_layer(c, l, s_before):
     # o_proj partial
     part = b(c.ws_o[l][: m * H * 2].view(torch.bfloat16).view(m, H))
     acc, absacc = oracle.gemm_f64(xb, wo)
-    check_gemm(part, oracle.gemm_bf16(xb, wo), acc, absacc, H, _splits(m, H, H))
+    check_gemm(part, oracle.gemm_bf16(xb, wo), acc, absacc, H, _splits(m, H, H),
+               label=f"chain M={m} layer {l} o_proj [8192,8192]")
     # dual norm on the GPU's partial and the stream before this layer
     s_ref, u_ref = oracle.dual_norm(part, s_before, b(c.post_w[l]), c.alpha, b(c.beta[l]),
                                     b(c.pre_w[l]), c.eps, c.eps)
@@ -50,7 +51,8 @@ def check_layer(c, l, s_before):
     ub, wp = b(c.u[l]), b(c.w_p[l])
     y = b(c.ws_p[l][: m * P * 2].view(torch.bfloat16).view(m, P))
     acc, absacc = oracle.gemm_f64(ub, wp)
-    check_gemm(y, oracle.gemm_bf16(ub, wp), acc, absacc, H, _splits(m, P, H))
+    check_gemm(y, oracle.gemm_bf16(ub, wp), acc, absacc, H, _splits(m, P, H),
+               label=f"chain M={m} layer {l} pooler [4096,8192]")
     gs = float(c.gs[l].item())
     z_tf = oracle.rmsnorm_bf16(y, b(c.norm_w[l]), c.eps, c.gc)
     assert ulp_distance(b(c.z[l]), z_tf).max() <= 1
@@ -62,7 +64,8 @@ def check_layer(c, l, s_before):
     # unpooler on the GPU's z
     zb, wu = b(c.z[l]), b(c.w_u[l])
     acc, absacc = oracle.gemm_f64(zb, wu)
-    check_gemm(b(c.h[l + 1]), oracle.gemm_bf16(zb, wu), acc, absacc, P, _splits(m, H, P))
+    check_gemm(b(c.h[l + 1]), oracle.gemm_bf16(zb, wu), acc, absacc, P, _splits(m, H, P),
+               label=f"chain M={m} layer {l} unpooler [8192,4096]")
 
 
 def _splits(m, n, k):
@@ -95,7 +98,7 @@ def test_graph_replay_equals_eager(chain):
     torch.cuda.synchronize()
     eager = (c.h[c.L].clone(), c.a.clone(), c.a_sf.clone(), c.s.clone())
     g = c.capture(c.forward)          # runs once eagerly, then captures
-    for _ in range(3):
+    for _ in range(100):
         c.set_input(c.h0, c.s0)
         g.replay()
         torch.cuda.synchronize()

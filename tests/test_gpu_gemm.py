@@ -85,7 +85,7 @@ def test_small_shapes_all_splits(sk, m, n, k):
         if k % (64 * splits):
             continue
         y = run(sk, x, w, splits)
-        check_gemm(y, yref, acc, absacc, k, splits)
+        check_gemm(y, yref, acc, absacc, k, splits, label=f"small M={m} [{n},{k}] S={splits}")
 
 
 def test_unpooler_shard_m1(sk):
@@ -94,7 +94,7 @@ def test_unpooler_shard_m1(sk):
     yref, acc, absacc = ref(x, w)
     s = sk.gemm_splits(1, 1024, 4096)
     y = run(sk, x, w)
-    check_gemm(y, yref, acc, absacc, 4096, s)
+    check_gemm(y, yref, acc, absacc, 4096, s, label=f"unpooler shard M=1 [1024,4096] S={s}")
     assert ulp_distance(y, yref).max() <= 1
 
 
@@ -109,7 +109,8 @@ def test_sweep_m_and_splits(sk, n, k):
             y = sk.gemm_bf16(x.to(DEV), wd, splits=splits)
             torch.cuda.synchronize()
             s = splits or sk.gemm_splits(m, n, k)
-            check_gemm(synth.bits(y), yref, acc, absacc, k, s)
+            check_gemm(synth.bits(y), yref, acc, absacc, k, s,
+                       label=f"sweep M={m} [{n},{k}] S={splits or f'auto({s})'}")
 
 
 @pytest.mark.parametrize("m,n,k", [(16, 24576, 2048), (4, 1024, 32768), (16, 8192, 16384)])
@@ -121,7 +122,8 @@ def test_large_shapes_sampled(sk, m, n, k):
     y = run(sk, x, w)
     cols = np.arange(0, n, 61)
     yref, acc, absacc = ref(x, w[torch.as_tensor(cols)])
-    check_gemm(y[:, cols], yref, acc, absacc, k, sk.gemm_splits(m, n, k))
+    check_gemm(y[:, cols], yref, acc, absacc, k, sk.gemm_splits(m, n, k),
+               label=f"large M={m} [{n},{k}] sampled 1/61")
 
 
 @pytest.mark.parametrize("n2,k2", [(4096, 8192), (1024, 512)])
