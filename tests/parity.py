@@ -10,7 +10,7 @@ Tolerances (stated here and in the design notes):
   accumulation of K/(16 S) sequential tensor-core steps of 16 products each,
   plus the S-term split sum. (ii) only matters where the exact result is
   tiny next to the summands (cancellation); the fraction of elements that
-  need it must stay below 2e-3.
+  need it must stay below 2e-4 (the worst case seen on GB300 is 6.9e-5).
 * BF16 norm outputs computed from the same input: ordered-bits distance <= 1
   (FP32 on the GPU against FP64 in the oracle, one rounding each).
 * FP32 residual: |gpu - ref| <= 1e-5 * (|alpha s| + |beta q|) per element.
@@ -56,7 +56,7 @@ def gemm_gamma(k: int, splits: int) -> float:
 GEMM_RECORDS: list = []
 
 
-def check_gemm(y_gpu_bits, y_ref_bits, acc, absacc, k: int, splits: int, max_frac_ii: float = 2e-3,
+def check_gemm(y_gpu_bits, y_ref_bits, acc, absacc, k: int, splits: int, max_frac_ii: float = 2e-4,
                label: str | None = None):
     """Asserts the GEMM tolerance; returns (n_strict_fail, n_total, max_ulp).
     n_strict_fail counts the outputs more than one BF16 ulp from the oracle's
