@@ -361,25 +361,81 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // ----------------------------------------------------------------------------
-// RMS factor of a row held by one CTA: the FP32 sum of v over the block in a
-// fixed order (shuffle-down tree inside each warp, then the warp totals in a
-// second shuffle-down tree in warp 0), and 1 / sqrt(sum / n + eps) computed
-// once with IEEE operations and handed to every thread. `red` holds >= 33
-// floats of shared memory.
-__device__ __forceinline__ float block_rms_inv(float v, float *red, float n, float eps) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_down_sync(0xffffffffu, v, off);
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    float t = lane < static_cast<int>(blockDim.x >> 5) ? red[lane] : 0.0f;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) t += __shfl_down_sync(0xffffffffu, t, off);
-    if (lane == 0) red[32] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, n), eps)));
+// Row reductions of the norm kernels. A token row is spread over a cluster of
+// C CTAs (column chunks, one CTA per rank); each row sum is taken in a fixed
+// order: each thread's own columns in column order, a shuffle-down tree inside
+// each warp, the warp totals in warp order, then the CTA totals in rank order
+// 0..C-1. Every rank pushes its CTA total into slot `rank` of every peer's
+// shared memory with st.async (completing 4 bytes on the peer's mbarrier of
+// that reduction), so each CTA ends with the same C values and forms the same
+// sum. The order depends only on the row width and the launch shape, so the
+// results are bitwise reproducible.
+constexpr int kNormMaxCluster = 8;
+constexpr int kNormReductions = 2;  // the dual norm takes two row sums
+
+struct NormShared {
+  uint64_t bar[kNormReductions];               // one mbarrier per row sum
+  float part[kNormReductions][kNormMaxCluster];  // CTA totals by rank
+  float red[32];                               // warp totals
+  uint32_t abort;                              // a bounded wait ran out
+};
+
+// Initialises the exchange barriers (thread 0) and starts the cluster barrier
+// that tells peers they may push (completed by norm_cluster_sum's first call).
+__device__ __forceinline__ void norm_exchange_init(NormShared &sh, int C, int nred) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nred; ++i) {
+      mbar_init(smem_u32(&sh.bar[i]), 1);
+      // this CTA's single arrival, plus the bytes its C - 1 peers push
+      mbar_arrive_expect_tx(smem_u32(&sh.bar[i]), static_cast<uint32_t>(4 * (C - 1)));
+    }
+    sh.abort = 0;
+    fence_barrier_init();
   }
   __syncthreads();
-  return red[32];
+  if (C > 1) cluster_arrive();
+}
+
+// Sum of v over the CTA (every thread's v), then over the cluster's ranks in
+// rank order; returned to every thread. `i` selects the reduction (its barrier
+// and slots); the first call also completes the cluster barrier started by
+// norm_exchange_init (peers' barriers are initialised before any push).
+__device__ __forceinline__ float norm_cluster_sum(NormShared &sh, float v, int C, int i, bool first) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = static_cast<int>(blockDim.x >> 5);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_down_sync(0xffffffffu, v, off);
+  if (nw > 1) {
+    if (lane == 0) sh.red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      v = lane < nw ? sh.red[lane] : 0.0f;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_down_sync(0xffffffffu, v, off);
+    }
+  }
+  const uint32_t rank = C > 1 ? cluster_ctarank() : 0;
+  if (C > 1 && first) cluster_wait();
+  if (threadIdx.x == 0) {
+    sh.part[i][rank] = v;
+    for (int q = 0; q < C; ++q) {
+      if (q == static_cast<int>(rank)) continue;
+      st_async_f32(dsmem_map(smem_u32(&sh.part[i][rank]), static_cast<uint32_t>(q)), v,
+                   dsmem_map(smem_u32(&sh.bar[i]), static_cast<uint32_t>(q)));
+    }
+  }
+  __syncthreads();  // this CTA's own slot is written; warp totals may be reused
+  if (C > 1 && !mbar_wait_bounded(smem_u32(&sh.bar[i]), 0, kWaitLimitNs)) {
+    atomicOr(&g_device_status, SK_DEVICE_WAIT_EPILOGUE);
+    sh.abort = 1;
+  }
+  float t = 0.0f;
+  for (int q = 0; q < C; ++q) t += sh.part[i][q];
+  return t;
+}
+
+__device__ __forceinline__ float rms_inv(float sum, float n, float eps) {
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(sum, n), eps)));
 }
 
 __device__ __forceinline__ void unpack8(const uint4 &v, uint16_t (&o)[8]) {
@@ -425,20 +481,22 @@ __device__ __forceinline__ uint32_t nvfp4_block16(const uint16_t (&z)[16], float
 }
 
 // Pre-expert RMSNorm + NVFP4 (cutedsl/moe/pooler_gather, module docstring;
-// pooler_layer: weight applied after the norm). One CTA per token row; each
-// thread owns one 16-column NVFP4 block. With a == NULL the NVFP4 step is
-// skipped and only z is stored: the norm of a BF16 edge layer (same page,
-// module docstring, ExpertsInputBf16).
+// pooler_layer: weight applied after the norm). Grid (C, m), cluster (C, 1, 1):
+// the C CTAs of a cluster share token row blockIdx.y, each thread owns one
+// 16-column NVFP4 block (CTA r: blocks r * blockDim.x + threadIdx.x). With
+// a == NULL the NVFP4 step is skipped and only z is stored: the norm of a BF16
+// edge layer (same page, module docstring, ExpertsInputBf16).
 __global__ void __launch_bounds__(1024)
     rmsnorm_nvfp4_kernel(const uint16_t *__restrict__ y, const uint16_t *__restrict__ norm_w,
                          float eps, float gc, const float *__restrict__ gs_ptr,
                          uint8_t *__restrict__ a, uint8_t *__restrict__ a_sf,
-                         uint16_t *__restrict__ z_out, int n) {
-  __shared__ float red[33];
+                         uint16_t *__restrict__ z_out, int n, int C) {
+  __shared__ NormShared sh;
   const int row = blockIdx.y;
-  const int blk = threadIdx.x;
+  const int blk = blockIdx.x * blockDim.x + threadIdx.x;
   const bool active = blk < (n >> 4);
   griddep_launch_dependents();
+  norm_exchange_init(sh, C, 1);
 
   uint16_t w[16];
   if (active) {  // the norm weight is never written by a kernel: read it before the wait
@@ -452,7 +510,9 @@ __global__ void __launch_bounds__(1024)
       w[8 + j] = hi[j];
     }
   }
+  float gsv = 0.0f;
   griddep_wait();
+  if (a && active) gsv = *gs_ptr;
 
   uint16_t v[16];
   float ss = 0.0f;
@@ -472,9 +532,9 @@ __global__ void __launch_bounds__(1024)
       ss = __fmaf_rn(f, f, ss);
     }
   }
-  const float r = block_rms_inv(ss, red, static_cast<float>(n), eps);
+  const float r = rms_inv(norm_cluster_sum(sh, ss, C, 0, true), static_cast<float>(n), eps);
 
-  if (active) {
+  if (active && !sh.abort) {
     uint16_t z[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -484,7 +544,7 @@ __global__ void __launch_bounds__(1024)
     const size_t base = static_cast<size_t>(row) * n + 16 * blk;
     if (a) {  // NVFP4 layers; a BF16 edge layer stores z only
       uint2 packed;
-      const uint32_t sf = nvfp4_block16(z, *gs_ptr, packed);
+      const uint32_t sf = nvfp4_block16(z, gsv, packed);
       reinterpret_cast<uint2 *>(a)[base >> 4] = packed;
       a_sf[base >> 4] = static_cast<uint8_t>(sf);
     }
@@ -527,29 +587,30 @@ __global__ void __launch_bounds__(256)
   a_sf[base >> 4] = static_cast<uint8_t>(sf);
 }
 
-// Attention-boundary dual norm (cutedsl/oproj/batt, AttentionBoundary). One
-// CTA per token row; each thread owns 8 consecutive columns. The elementwise
-// steps use the packed FP32x2 operations (each lane an IEEE round-to-nearest
-// operation, the same as the scalar one) to halve the instruction count of a
-// row that one SM works through alone.
-constexpr int kDualThreads = 1024;
-
+// Attention-boundary dual norm (cutedsl/oproj/batt, AttentionBoundary). Grid
+// (C, m), cluster (C, 1, 1): the C CTAs of a cluster share token row
+// blockIdx.y, each thread owns 8 consecutive columns (CTA r: chunks
+// r * blockDim.x + threadIdx.x). The two row sums (of the partial, then of the
+// updated residual) are cluster reductions. The elementwise steps use the
+// packed FP32x2 operations (each lane an IEEE round-to-nearest operation, the
+// same as the scalar one).
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 // the two BF16 of a 32-bit word as FP32 (low half first)
 __device__ __forceinline__ float2 bf16x2_f2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
 
-__global__ void __launch_bounds__(kDualThreads)
+__global__ void __launch_bounds__(1024)
     dual_norm_kernel(const uint16_t *__restrict__ p, float *__restrict__ s,
                      const uint16_t *__restrict__ w1, float alpha,
                      const uint16_t *__restrict__ beta, const uint16_t *__restrict__ w2,
                      uint16_t *__restrict__ out, float eps_post, float eps_pre, float gc_post,
-                     float gc_pre, int h) {
-  __shared__ float red1[33], red2[33];
+                     float gc_pre, int h, int C) {
+  __shared__ NormShared sh;
   const int row = blockIdx.y;
-  const int ch = threadIdx.x;
+  const int ch = blockIdx.x * blockDim.x + threadIdx.x;
   const bool active = ch < (h >> 3);
   griddep_launch_dependents();
+  norm_exchange_init(sh, C, 2);
 
   // Weights first (never written by a kernel), then wait for the producer of
   // the partial and of the residual stream.
@@ -582,7 +643,7 @@ __global__ void __launch_bounds__(kDualThreads)
       ss1 = __fmaf_rn(pv[j].y, pv[j].y, ss1);
     }
   }
-  const float r1 = block_rms_inv(ss1, red1, static_cast<float>(h), eps_post);
+  const float r1 = rms_inv(norm_cluster_sum(sh, ss1, C, 0, true), static_cast<float>(h), eps_post);
 
   float ss2 = 0.0f;
   if (active) {
@@ -598,13 +659,15 @@ __global__ void __launch_bounds__(kDualThreads)
       ss2 = __fmaf_rn(sv[j].x, sv[j].x, ss2);
       ss2 = __fmaf_rn(sv[j].y, sv[j].y, ss2);
     }
-    float4 *sp = reinterpret_cast<float4 *>(s + rbase) + 2 * ch;
-    sp[0] = make_float4(sv[0].x, sv[0].y, sv[1].x, sv[1].y);
-    sp[1] = make_float4(sv[2].x, sv[2].y, sv[3].x, sv[3].y);
+    if (!sh.abort) {
+      float4 *sp = reinterpret_cast<float4 *>(s + rbase) + 2 * ch;
+      sp[0] = make_float4(sv[0].x, sv[0].y, sv[1].x, sv[1].y);
+      sp[1] = make_float4(sv[2].x, sv[2].y, sv[3].x, sv[3].y);
+    }
   }
-  const float r2 = block_rms_inv(ss2, red2, static_cast<float>(h), eps_pre);
+  const float r2 = rms_inv(norm_cluster_sum(sh, ss2, C, 1, false), static_cast<float>(h), eps_pre);
 
-  if (active) {
+  if (active && !sh.abort) {
     const uint32_t w2w[4] = {g2.x, g2.y, g2.z, g2.w};
     const float2 r2v = make_float2(r2, r2), gcv = make_float2(gc_pre, gc_pre);
     uint16_t o[8];
@@ -790,13 +853,26 @@ cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, ui
                    dim3(1, splits, 1), tmap_w, tmap_x, a.pf_stages ? pf->map : tmap_w, a);
 }
 
+// Cluster size and CTA width of a norm over `units` per row (NVFP4 blocks or
+// 8-column chunks): up to kNormMaxCluster CTAs per row, each with at least
+// `min_per_cta` units, whole warps.
+static void norm_shape(int units, int min_per_cta, int *C, int *threads) {
+  int c = (units + min_per_cta - 1) / min_per_cta;
+  c = c < 1 ? 1 : (c > kNormMaxCluster ? kNormMaxCluster : c);
+  const int per = (units + c - 1) / c;
+  *C = c;
+  *threads = (per + 31) / 32 * 32;
+}
+
 cudaError_t launch_rmsnorm_nvfp4(const uint16_t *y, const uint16_t *norm_w, float eps, float gc,
                                  const float *gs, uint8_t *a, uint8_t *a_sf, uint16_t *z_out,
                                  int m, int n, cudaStream_t stream, bool pdl) {
-  // one CTA per token row, one thread per 16-column block (n <= 16384)
-  const int threads = (n / 16 + 31) / 32 * 32;
-  return launch_ex(rmsnorm_nvfp4_kernel, dim3(1, m), dim3(threads), 0, stream, pdl, dim3(1, 1, 1),
-                   y, norm_w, eps, gc, gs, a, a_sf, z_out, n);
+  // one thread per 16-column block, a cluster of CTAs per token row
+  // (n <= 16384: at most 1024 blocks over at most 8 CTAs)
+  int C, threads;
+  norm_shape(n / 16, 32, &C, &threads);
+  return launch_ex(rmsnorm_nvfp4_kernel, dim3(C, m), dim3(threads), 0, stream, pdl, dim3(C, 1, 1),
+                   y, norm_w, eps, gc, gs, a, a_sf, z_out, n, C);
 }
 
 cudaError_t launch_nvfp4_quantize(const uint16_t *z, const float *gs, uint8_t *a, uint8_t *a_sf,
@@ -811,11 +887,12 @@ cudaError_t launch_dual_norm(const uint16_t *p, float *s, const uint16_t *w1, fl
                              const uint16_t *beta, const uint16_t *w2, uint16_t *out,
                              float eps_post, float eps_pre, float gc_post, float gc_pre, int m,
                              int h, cudaStream_t stream, bool pdl) {
-  // one CTA per token row, 8 columns per thread (h <= 8 * kDualThreads is
-  // checked by the caller)
-  const int threads = (h / 8 + 31) / 32 * 32;
-  return launch_ex(dual_norm_kernel, dim3(1, m), dim3(threads), 0, stream, pdl, dim3(1, 1, 1), p, s,
-                   w1, alpha, beta, w2, out, eps_post, eps_pre, gc_post, gc_pre, h);
+  // 8 columns per thread, a cluster of CTAs per token row (h <= 8192 is
+  // checked by the caller: at most 1024 chunks over at most 8 CTAs)
+  int C, threads;
+  norm_shape(h / 8, 128, &C, &threads);
+  return launch_ex(dual_norm_kernel, dim3(C, m), dim3(threads), 0, stream, pdl, dim3(C, 1, 1), p,
+                   s, w1, alpha, beta, w2, out, eps_post, eps_pre, gc_post, gc_pre, h, C);
 }
 
 cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t stream) {

@@ -281,6 +281,15 @@ __device__ __forceinline__ void st_async_v4_f32(uint32_t caddr, float a, float b
       : "memory");
 }
 
+// One FP32 into a peer CTA's shared memory (4-byte aligned cluster address);
+// the 4 bytes count toward the transaction bytes of the peer's mbarrier.
+__device__ __forceinline__ void st_async_f32(uint32_t caddr, float v, uint32_t cbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                   caddr),
+               "r"(__float_as_uint(v)), "r"(cbar)
+               : "memory");
+}
+
 // Split cluster barrier: arrive (release) now, wait (acquire) later.
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");

@@ -215,6 +215,39 @@ def test_dual_norm_small_width_and_alpha(sk):
     assert ulp_distance(synth.bits(out), out_ref).max() <= 1
 
 
+@pytest.mark.parametrize("h", [8, 72, 1032, 4096, 8184])
+def test_dual_norm_row_widths(sk, h):
+    # widths that spread a row over 1, 2, 4 and 8 CTAs, with a partly idle last CTA
+    g = torch.Generator().manual_seed(h)
+    m = 5
+    p = (torch.randn(m, h, generator=g) * 1.3).to(torch.bfloat16)
+    s = torch.randn(m, h, generator=g)
+    beta = (0.5 + torch.rand(h, generator=g)).to(torch.bfloat16)
+    w1 = (1 + 0.1 * torch.randn(h, generator=g)).to(torch.bfloat16)
+    w2 = (1 + 0.1 * torch.randn(h, generator=g)).to(torch.bfloat16)
+    s_dev = s.to(DEV)
+    out = sk.dual_norm_residual(p.to(DEV), s_dev, w1.to(DEV), 1.0, beta.to(DEV), w2.to(DEV))
+    torch.cuda.synchronize()
+    d = dict(alpha=1.0, beta=beta, pre_w=w2, eps=1e-6)
+    _check_dual(sk, d, synth.bits(p), s.numpy(), s_dev.cpu().numpy(), out, w1)
+
+
+@pytest.mark.parametrize("n", [16, 1040, 4112, 16368])
+def test_rmsnorm_nvfp4_row_widths(sk, n):
+    # widths that spread a row over 1, 3, 8 CTAs (ragged last CTA)
+    m = 3
+    y = synth.normal_bf16((m, n), 1.8, n)
+    w = synth.normal_bf16((n,), 0.1, n + 1)
+    gs = 2688.0 / 7.0
+    a, a_sf, z = sk.rmsnorm_nvfp4(y.to(DEV), w.to(DEV), synth.EPS, synth.GAIN_CENTER, gs_tensor(gs),
+                                  z_out=True)
+    torch.cuda.synchronize()
+    z_ref = oracle.rmsnorm_bf16(synth.bits(y), synth.bits(w), synth.EPS, synth.GAIN_CENTER)
+    assert ulp_distance(synth.bits(z), z_ref).max() <= 1
+    a_ref, sf_ref = oracle.nvfp4_quantize(synth.bits(z), gs)
+    assert np.array_equal(a.cpu().numpy(), a_ref) and np.array_equal(a_sf.cpu().numpy(), sf_ref)
+
+
 @pytest.mark.parametrize("b", [1, 4, 16])
 def test_oproj_gemm_dual_norm(sk, b):
     d = synth.oproj_boundary(b)
