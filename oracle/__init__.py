@@ -18,6 +18,10 @@ specialized decode):
 * ``nvfp4_quantize``: cutedsl/moe/pooler_gather, module docstring (NVFP4 layout),
   cvt_e2m1x8_f32, cvt_f32_to_e4m3, nvfp4_compute_output_scale.
 * ``dual_norm``: cutedsl/oproj/batt, AttentionBoundary.
+* ``nvfp4_dequant`` / ``gemm_nvfp4w``: not on the pages. The weight-only
+  NVFP4 GEMM holds W [n, k] in the NVFP4 layout of the pooler page's module
+  docstring (codes two per byte, even column low nibble; one e4m3 scale per
+  16 columns of a row) with one FP32 multiplier ``w_scale``.
 
 Parity pins: every function here is pinned by ``tests/test_oracle_*.py``
 against closed forms, library routines (torch's float8/bfloat16 casts),
@@ -87,7 +91,10 @@ def _load():
         lib.oracle_dual_norm.argtypes = [u16p, f32p, vp, d, u16p, u16p, u16p,
                                          d, d, d, d, vp, vp, i, i]
         lib.oracle_dual_norm.restype = None
-        _ = (f64p,)
+        lib.oracle_nvfp4_dequant.argtypes = [u8p, u8p, f64p, i, i]
+        lib.oracle_nvfp4_dequant.restype = None
+        lib.oracle_gemm_nvfp4w.argtypes = [u16p, u8p, u8p, ctypes.c_float, vp, vp, vp, i, i, i]
+        lib.oracle_gemm_nvfp4w.restype = None
         _lib = lib
         return lib
 
@@ -223,3 +230,34 @@ def dual_norm(partial, stream, post_w, alpha: float, beta, pre_w, eps_post: floa
                              _f32(eps_post), _f32(eps_pre), _f32(gc_post),
                              _f32(gc_pre), _ptr(r1), _ptr(r2), m, h)
     return (s, out, r1, r2) if return_r else (s, out)
+
+
+# ------------------------------------------------- weight-only NVFP4 GEMM ----
+def nvfp4_dequant(wq, wsf) -> np.ndarray:
+    """dq [n, k] float64: e2m1(code) * e4m3(block scale) of NVFP4 weight bytes
+    wq [n, k/2] (column 2c in the low nibble) and wsf [n, k/16] (exact)."""
+    wq = np.ascontiguousarray(wq, dtype=np.uint8)
+    wsf = np.ascontiguousarray(wsf, dtype=np.uint8)
+    n, kh = wq.shape
+    k = 2 * kh
+    assert k % 16 == 0 and wsf.shape == (n, k // 16)
+    dq = np.empty((n, k), np.float64)
+    _load().oracle_nvfp4_dequant(wq, wsf, dq, n, k)
+    return dq
+
+
+def gemm_nvfp4w(x, wq, wsf, w_scale: float, return_acc: bool = False):
+    """y [m, n] BF16 bits = bf16_rn(w_scale * sum_k x[m,k] dq[n,k]), -0 stored as
+    +0; with ``return_acc`` also (acc, absacc): w_scale * sum and
+    |w_scale| * sum |x dq| in float64."""
+    x = _u16(x)
+    wq = np.ascontiguousarray(wq, dtype=np.uint8)
+    wsf = np.ascontiguousarray(wsf, dtype=np.uint8)
+    m, k = x.shape
+    n = wq.shape[0]
+    assert wq.shape == (n, k // 2) and wsf.shape == (n, k // 16) and k % 16 == 0
+    y = np.empty((m, n), np.uint16)
+    acc = np.empty((m, n), np.float64)
+    absacc = np.empty((m, n), np.float64)
+    _load().oracle_gemm_nvfp4w(x, wq, wsf, _f32(w_scale), _ptr(y), _ptr(acc), _ptr(absacc), m, n, k)
+    return (y, acc, absacc) if return_acc else y

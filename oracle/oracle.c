@@ -51,6 +51,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* ------------------------------------------------------------------------- */
@@ -350,4 +351,64 @@ void oracle_dual_norm(const uint16_t *p, float *s, const uint16_t *w1, double al
         if (r2_out)
             r2_out[i] = r2;
     }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Weight-only NVFP4 GEMM. Not on the pages: the weight W [n, k] is held in  */
+/* the NVFP4 byte layout the pooler page's module docstring gives for the    */
+/* experts' input, applied to the rows of W along K: two e2m1 codes per byte */
+/* (column 2c in the low nibble), one float8_e4m3fn scale per 16 consecutive */
+/* columns of a row, and one FP32 dequantization multiplier w_scale for the  */
+/* whole tensor (the reciprocal of the global scale the codes were made      */
+/* with). Readings (also in the design notes): a weight element is           */
+/* e2m1(code) * e4m3(scale), exact in FP64; w_scale multiplies the finished  */
+/* sum once per output, as a per-tensor factor commutes with the sum.        */
+/* ------------------------------------------------------------------------- */
+
+/* dq[n, k] = e2m1 value of the code of W[n, k] times the e4m3 value of its
+   block scale (exact). wq is [n, k/2] bytes, wsf is [n, k/16] bytes. */
+void oracle_nvfp4_dequant(const uint8_t *wq, const uint8_t *wsf, double *dq, int n, int k)
+{
+    for (int r = 0; r < n; ++r) {
+        for (int j = 0; j < k; ++j) {
+            uint8_t byte = wq[(size_t)r * (k / 2) + j / 2];
+            uint8_t code = (j % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+            double sf = (double)oracle_e4m3_to_float(wsf[(size_t)r * (k / 16) + j / 16]);
+            dq[(size_t)r * k + j] = (double)oracle_e2m1_to_float(code) * sf;
+        }
+    }
+}
+
+/* y[m, n] = bf16_rn(w_scale * sum_k x[m, k] * dq[n, k]), -0.0 stored as +0.0.
+   The sum is taken in FP64 in k order, multiplied by w_scale in FP64 and
+   rounded once to BF16. acc (may be NULL) receives w_scale * sum, absacc (may
+   be NULL) |w_scale| * sum_k |x * dq| (the scale of the summation error). */
+void oracle_gemm_nvfp4w(const uint16_t *x, const uint8_t *wq, const uint8_t *wsf,
+                        float w_scale, uint16_t *y, double *acc, double *absacc,
+                        int m, int n, int k)
+{
+    double *dq = (double *)malloc(sizeof(double) * (size_t)n * k);
+    if (!dq)
+        return;
+    oracle_nvfp4_dequant(wq, wsf, dq, n, k);
+    for (int i = 0; i < m; ++i) {
+        for (int r = 0; r < n; ++r) {
+            const uint16_t *xr = x + (size_t)i * k;
+            const double *wr = dq + (size_t)r * k;
+            double s = 0.0, sa = 0.0;
+            for (int t = 0; t < k; ++t) {
+                double p = oracle_bf16_to_double(xr[t]) * wr[t];
+                s += p;
+                sa += fabs(p);
+            }
+            double v = (double)w_scale * s;
+            if (y)
+                y[(size_t)i * n + r] = bf16_store(v);
+            if (acc)
+                acc[(size_t)i * n + r] = v;
+            if (absacc)
+                absacc[(size_t)i * n + r] = fabs((double)w_scale) * sa;
+        }
+    }
+    free(dq);
 }
