@@ -248,6 +248,42 @@ sk_status sk_gemm_dual_norm(const void *x, const void *w, float *resid, const vo
                             void *workspace, size_t workspace_bytes, int m, int n, int k,
                             int splits, void *stream);
 
+/*
+ * sk_gemm_nvfp4w_bf16 -- weight-only NVFP4 GEMM:
+ *   y[m, n] = bf16_rn( w_scale * sum_k x[m, k] * W[n, k] ),
+ *   W[n, k] = e2m1(code[n, k]) * e4m3(wsf[n, k / 16])
+ * No counterpart on the pages: the weight is held in the NVFP4 byte layout that
+ * cutedsl/moe/pooler_gather (module docstring) gives for the experts' input,
+ * applied to the rows of W along K, so the GEMM streams 4.5 bits per weight
+ * instead of 16. sk_nvfp4_quantize of a BF16 weight [n, k] with global scale
+ * gs produces (wq, wsf), with w_scale = 1 / gs.
+ *   x        BF16 [m, k] activations, 1 <= m <= 16
+ *   wq       u8 [n, k/2]: e2m1 codes, column 2c in the low nibble, 2c+1 high
+ *   wsf      u8 [n, k/16]: float8_e4m3fn scale of each 16 columns of a row,
+ *            row-major, not swizzled (NaN encodings are out of contract)
+ *   w_scale  device FP32 [1], multiplies the sum (read after the kernel ahead
+ *            in the stream completes)
+ *   y        BF16 [m, n] output; -0.0 is stored as +0.0
+ *   n % 16 == 0, k % 256 == 0, splits 0 (automatic) or 1, 2, 4, 8, 16 with
+ *   k % (256 * splits) == 0; x, wq, wsf, y 16-byte aligned.
+ * Each weight is expanded exactly to BF16 on chip (code * scale has at most
+ * six significant bits); the products are accumulated in FP32 on the tensor
+ * cores, the split partials summed in split order, the sum multiplied by
+ * w_scale in FP32 and rounded once to BF16. Bitwise reproducible for a given
+ * (m, n, k, splits).
+ */
+sk_status sk_gemm_nvfp4w_bf16(const void *x, const uint8_t *wq, const uint8_t *wsf,
+                              const float *w_scale, void *y, int m, int n, int k, int splits,
+                              void *stream);
+
+/* Why (m, n, k, splits) has no weight-only NVFP4 GEMM launch, or SK_OK
+   (host-only). */
+sk_status sk_gemm_nvfp4w_supported(int m, int n, int k, int splits);
+
+/* Split count the weight-only NVFP4 GEMM uses for (m, n, k, splits) on the
+   current device (splits itself when nonzero); 0 if the shape has no launch. */
+int sk_gemm_nvfp4w_splits(int m, int n, int k, int splits);
+
 /* Bytes of the static device scratch behind sk_gemm_rmsnorm_nvfp4_static:
    room for a BF16 [m, n] GEMM output with m * n <= 131072 (16 x 8192). */
 #define SK_STATIC_SCRATCH_BYTES (16u * 8192u * 2u)

@@ -78,6 +78,9 @@ def lib() -> ctypes.CDLL:
             "sk_gemm_dual_norm_workspace": ([i, i], sz),
             "sk_gemm_dual_norm": ([vp, vp, vp, vp, f, vp, vp, vp, f, f, f, f, vp, sz, i, i, i, i, vp], i),
             "sk_gemm_rmsnorm_nvfp4_static": ([vp, vp, vp, f, f, vp, vp, vp, vp, i, i, i, i, vp], i),
+            "sk_gemm_nvfp4w_bf16": ([vp, vp, vp, vp, vp, i, i, i, i, vp], i),
+            "sk_gemm_nvfp4w_supported": ([i, i, i, i], i),
+            "sk_gemm_nvfp4w_splits": ([i, i, i, i], i),
             "sk_device_status": ([ctypes.POINTER(ctypes.c_uint32), i], i),
             "sk_convert_probe": ([i, vp, vp, i, vp], i),
             "sk_wait_probe": ([ctypes.c_uint, vp], i),
@@ -354,6 +357,38 @@ def gemm_dual_norm(x, w, resid, post_w, alpha: float, beta, pre_w, out=None,
         eps_post, eps_pre, gc_post, gc_pre, _ptr(workspace),
         workspace.numel() * workspace.element_size(), m, n, k, splits, _stream(stream)))
     return out, workspace
+
+
+# ------------------------------------------------- weight-only NVFP4 GEMM ----
+def gemm_nvfp4w_supported(m: int, n: int, k: int, splits: int = 0) -> str | None:
+    """None if the weight-only NVFP4 GEMM has a launch for the shape, else why."""
+    st = lib().sk_gemm_nvfp4w_supported(m, n, k, splits)
+    return None if st == SK_OK else last_error()
+
+
+def gemm_nvfp4w_splits(m: int, n: int, k: int, splits: int = 0) -> int:
+    s = int(lib().sk_gemm_nvfp4w_splits(m, n, k, splits))
+    if s == 0:
+        raise SkValueError(SK_ERR_UNSUPPORTED, last_error())
+    return s
+
+
+def gemm_nvfp4w(x, wq, wsf, w_scale, out=None, splits: int = 0, stream=None):
+    """out[m, n] = bf16(w_scale * x[m, k] @ W^T), W[n, k] = e2m1(wq) * e4m3(wsf):
+    wq uint8 [n, k/2] (column 2c in the low nibble), wsf uint8 [n, k/16]
+    (float8_e4m3fn bits), w_scale float32 [1] on the device."""
+    m, k = x.shape
+    n = wq.shape[0]
+    _need(x, torch.bfloat16, (m, k), "x")
+    _need(wq, torch.uint8, (n, k // 2), "wq")
+    _need(wsf, torch.uint8, (n, k // 16), "wsf")
+    _need(w_scale, torch.float32, (1,), "w_scale")
+    if out is None:
+        out = torch.empty(m, n, dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, (m, n), "out")
+    _check(lib().sk_gemm_nvfp4w_bf16(_ptr(x), _ptr(wq), _ptr(wsf), _ptr(w_scale), _ptr(out), m, n,
+                                     k, splits, _stream(stream)))
+    return out
 
 
 # ----------------------------------------------------------- diagnostics ----

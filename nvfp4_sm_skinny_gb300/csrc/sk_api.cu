@@ -100,6 +100,28 @@ sk_status make_map(CUtensorMap *map, const void *base, int rows, int cols, int b
   return SK_OK;
 }
 
+// Tensor map of NVFP4 weight bytes [rows, row_bytes] seen as three dimensions
+// {box_bytes, rows, row_bytes / box_bytes}: one box is box_bytes of each of
+// `box_rows` rows of one K block, 128-byte swizzled when `swizzle` (the code
+// tile whose rows the expansion warps read) or plain (the scale tile). Rows
+// past `rows` read as zero.
+sk_status make_byte_map(CUtensorMap *map, const void *base, int rows, int row_bytes, int box_bytes,
+                        int box_rows, bool swizzle) {
+  auto fn = encode_fn();
+  if (!fn) return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(box_bytes), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(row_bytes / box_bytes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(box_bytes)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_bytes), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return SK_OK;
+}
+
 sk_status check_gemm_shape(int m, int n, int k, int splits) {
   if (m < 1 || m > SK_MAX_M)
     return fail(SK_ERR_INVALID_ARG, "m=%d: needs 1 <= m <= %d token rows", m, SK_MAX_M);
@@ -287,6 +309,53 @@ sk_status check_ptrs16(const char *names, std::initializer_list<const void *> ps
 }
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+// ------------------------------------------------- weight-only NVFP4 GEMM
+sk_status check_nvfp4w_shape(int m, int n, int k, int splits) {
+  if (m < 1 || m > SK_MAX_M)
+    return fail(SK_ERR_INVALID_ARG, "m=%d: needs 1 <= m <= %d token rows", m, SK_MAX_M);
+  if (n <= 0 || n % 16)
+    return fail(SK_ERR_INVALID_ARG, "n=%d: needs a positive multiple of 16 output features", n);
+  if (k <= 0 || k % sk::kW4BlockK)
+    return fail(SK_ERR_INVALID_ARG, "k=%d: needs a positive multiple of %d", k, sk::kW4BlockK);
+  if (splits != 0 && splits != 1 && splits != 2 && splits != 4 && splits != 8 && splits != 16)
+    return fail(SK_ERR_UNSUPPORTED, "unsupported split count %d (0, 1, 2, 4, 8 or 16)", splits);
+  if (splits > 0 && k % (sk::kW4BlockK * splits))
+    return fail(SK_ERR_UNSUPPORTED, "K=%d does not split into %d slices of whole %d-wide blocks", k,
+                splits, sk::kW4BlockK);
+  return SK_OK;
+}
+
+// Split count and ring depth of the weight-only NVFP4 GEMM. One CTA per SM
+// (each takes all of its SM's tensor memory): the largest S that keeps the
+// grid within one wave of resident clusters with at least two K blocks per
+// CTA; the ring as deep as shared memory allows.
+struct W4Plan {
+  int splits, stages;
+};
+
+W4Plan plan_nvfp4w(int n, int k, int splits_req, int device, int sm_count) {
+  W4Plan p{1, 1};
+  const int tiles = (n + sk::kW4Rows - 1) / sk::kW4Rows;
+  const int nblk = k / sk::kW4BlockK;
+  if (splits_req) {
+    p.splits = splits_req;
+  } else {
+    for (int s = 2; s <= 16; s *= 2) {
+      if (nblk % s || nblk / s < 2) break;
+      if (tiles * s > sm_count) break;
+      const int c = sk::w4_max_clusters(device, s);
+      if (c > 0 && tiles > c) break;
+      p.splits = s;
+    }
+  }
+  const int per = nblk / p.splits;
+  int st = 1;
+  while (st < sk::kW4MaxStages && sk::w4_smem_bytes(st + 1, p.splits) <= sk::kOnePerSmSmem) ++st;
+  if (const int sv = env_int("SK_STAGES", 1, sk::kW4MaxStages)) st = sv;
+  p.stages = st < per ? st : per;
+  return p;
+}
 
 }  // namespace
 
@@ -529,6 +598,49 @@ sk_status sk_gemm_dual_norm(const void *x, const void *w, float *resid, const vo
                            static_cast<uint16_t *>(out), eps_post, eps_pre, gc_post, gc_pre, m, n,
                            as_stream(stream), pdl_enabled()),
       "dual_norm");
+}
+
+sk_status sk_gemm_nvfp4w_supported(int m, int n, int k, int splits) {
+  sk_status st = check_nvfp4w_shape(m, n, k, splits);
+  return st == SK_OK ? ok() : st;
+}
+
+int sk_gemm_nvfp4w_splits(int m, int n, int k, int splits) {
+  if (check_nvfp4w_shape(m, n, k, splits) != SK_OK) return 0;
+  if (splits) return splits;
+  sk::DeviceInfo info;
+  if (current_device(&info) != SK_OK) return 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  ok();
+  return plan_nvfp4w(n, k, 0, dev, info.sm_count).splits;
+}
+
+sk_status sk_gemm_nvfp4w_bf16(const void *x, const uint8_t *wq, const uint8_t *wsf,
+                              const float *w_scale, void *y, int m, int n, int k, int splits,
+                              void *stream) {
+  sk_status st;
+  if ((st = check_nvfp4w_shape(m, n, k, splits)) != SK_OK) return st;
+  if ((st = check_ptrs16("sk_gemm_nvfp4w_bf16(x, wq, wsf, y)", {x, wq, wsf, y})) != SK_OK) return st;
+  if (!w_scale || (reinterpret_cast<uintptr_t>(w_scale) & 3))
+    return fail(SK_ERR_INVALID_ARG, "w_scale must be a 4-byte aligned device FP32 [1]");
+  sk::DeviceInfo info;
+  if ((st = current_device(&info)) != SK_OK) return st;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const W4Plan plan = plan_nvfp4w(n, k, splits, dev, info.sm_count);
+  CUtensorMap tq, tsf, tx;
+  if ((st = make_byte_map(&tq, wq, n, k / 2, 128, sk::kW4Rows, true)) != SK_OK) return st;
+  if ((st = make_byte_map(&tsf, wsf, n, k / 16, 16, sk::kW4Rows, false)) != SK_OK) return st;
+  if ((st = make_map(&tx, x, m, k, sk::kTokTile, sk::kW4BlockK / sk::kBlockK)) != SK_OK) return st;
+  // about 256 KiB of each CTA's code and scale blocks beyond the ring start
+  // towards L2 before the dependency wait
+  const int l2_ahead = (256 * 1024 + sk::kW4CodeBytes + sk::kW4ScaleBytes - 1) /
+                       (sk::kW4CodeBytes + sk::kW4ScaleBytes);
+  return launch_status(sk::launch_gemm_nvfp4w(tq, tsf, tx, w_scale, static_cast<uint16_t *>(y), m,
+                                              n, k, plan.splits, plan.stages, l2_ahead,
+                                              as_stream(stream), pdl_enabled()),
+                       "gemm_nvfp4w");
 }
 
 sk_status sk_wait_probe(unsigned limit_us, void *stream) {

@@ -87,6 +87,44 @@ __host__ __device__ inline GemmLayout gemm_layout(int h, int stages, int bps, in
   return L;
 }
 
+// Weight-only NVFP4 GEMM tiling. A CTA owns kW4Rows weight rows (the MMA's M)
+// and one K slice, moved in blocks of kW4BlockK columns: per block the copy
+// engine brings 128 code bytes and 16 scale bytes per row and the block's
+// 16 x 256 BF16 activations; dequantization warps expand the codes into BF16
+// tensor-memory operands (kW4ACols columns per block, kW4ABufs buffers).
+constexpr int kW4BlockK = 256;
+constexpr int kW4Rows = 128;
+constexpr int kW4CodeBytes = kW4Rows * kW4BlockK / 2;   // 16 KiB
+constexpr int kW4ScaleBytes = kW4Rows * kW4BlockK / 16; // 2 KiB
+constexpr int kW4XBytes = kTokTile * kW4BlockK * 2;     // 8 KiB
+constexpr int kW4StageBytes = kW4CodeBytes + kW4ScaleBytes + kW4XBytes;
+constexpr int kW4ABufs = 3;
+constexpr int kW4ACols = kW4BlockK / 2;                 // 128
+constexpr int kW4MaxStages = 8;
+// At least this much dynamic shared memory per CTA, so that two CTAs of the
+// kernel never share an SM (each allocates all of the SM's tensor memory).
+constexpr size_t kW4MinSmem = 116 * 1024;
+
+// Shared-memory layout of a weight-only NVFP4 GEMM CTA, from its 1024-aligned
+// base: code slots (16 KiB each, 128-byte swizzled rows), activation slots
+// (8 KiB), scale slots (2 KiB), the split-K exchange buffer, the mbarriers.
+struct W4Layout {
+  int x_off, sf_off, red_off, bar_off, total;
+};
+
+__host__ __device__ inline W4Layout w4_layout(int stages, int splits) {
+  W4Layout L;
+  L.x_off = stages * kW4CodeBytes;
+  L.sf_off = L.x_off + stages * kW4XBytes;
+  L.red_off = L.sf_off + stages * kW4ScaleBytes;
+  const int rows = splits > 1 ? splits * ((kW4Rows + splits - 1) / splits) : 0;
+  L.bar_off = L.red_off + rows * kTokTile * 4;
+  // full[stages], empty[stages], a_full[3], a_empty[3], done, exchange; then
+  // the TMEM address and an abort flag
+  L.total = L.bar_off + (2 * stages + 2 * kW4ABufs + 2) * 8 + 8;
+  return L;
+}
+
 struct DeviceInfo {
   int sm_count = 0;
   int major = 0, minor = 0;
@@ -124,6 +162,22 @@ cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, ui
                         int n, int k, int splits, int h, int stages, int bps, cudaStream_t stream,
                         bool pdl, const GemmPrefetch *pf = nullptr, int l2_ahead = -1,
                         bool x_ready = false);
+
+// Dynamic shared memory of a weight-only NVFP4 GEMM CTA.
+size_t w4_smem_bytes(int stages, int splits);
+
+// Largest number of clusters of `splits` weight-only NVFP4 GEMM CTAs that can
+// be resident at once (one CTA per SM; cached).
+int w4_max_clusters(int device, int splits);
+
+// Launches the weight-only NVFP4 GEMM: grid (ceil(n / 128), splits), cluster
+// (1, splits, 1). tmap_q: codes {128 bytes, n rows, k / 256 blocks}, box
+// {128, 128, 1}, 128-byte swizzle; tmap_sf: scales {16 bytes, n, k / 256},
+// box {16, 128, 1}; tmap_x: activations {64, m, k / 64}, box {64, 16, 4}.
+cudaError_t launch_gemm_nvfp4w(const CUtensorMap &tmap_q, const CUtensorMap &tmap_sf,
+                               const CUtensorMap &tmap_x, const float *w_scale, uint16_t *y,
+                               int m, int n, int k, int splits, int stages, int l2_ahead,
+                               cudaStream_t stream, bool pdl);
 
 cudaError_t launch_rmsnorm_nvfp4(const uint16_t *y, const uint16_t *norm_w, float eps, float gc,
                                  const float *gs, uint8_t *a, uint8_t *a_sf, uint16_t *z_out,

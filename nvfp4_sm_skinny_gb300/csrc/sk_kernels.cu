@@ -64,6 +64,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 // The values are staged as BF16 in shared memory, then each token's row
 // segment leaves in 16-byte stores (one per 8 features) instead of one 2-byte
 // store per token and feature. Called by all threads of the CTA.
+template <int NT>
 __device__ __forceinline__ void store_tile_rows(uint16_t *stage, const float (&v)[kTokTile], int r0,
                                                 int r1, uint16_t *y, int n, int n0, int m,
                                                 bool ok) {
@@ -74,12 +75,121 @@ __device__ __forceinline__ void store_tile_rows(uint16_t *stage, const float (&v
   }
   __syncthreads();
   const int per_t = nr >> 3;
-  for (int c = tid; c < m * per_t; c += kGemmThreads) {
+  for (int c = tid; c < m * per_t; c += NT) {
     const int t = c / per_t, q = c - t * per_t;
     const int row = n0 + r0 + 8 * q;
     if (ok && row < n)
       *reinterpret_cast<uint4 *>(y + static_cast<size_t>(t) * n + row) =
           *reinterpret_cast<const uint4 *>(stage + t * nr + 8 * q);
+  }
+}
+
+// The GEMM epilogue after the accumulators are read: the split-K exchange
+// between the S ranks of the cluster (S > 1), the optional output scale, the
+// BF16 rounding (-0 stored as +0) and the stores of the tile's rows
+// [n0, n0 + h) of y (threads 0..h-1 hold one row each in acc). `stage` is
+// idle shared memory for the row staging, `red` the exchange buffer counted on
+// `red_bar`. Called by all NT threads of the CTA.
+//
+// Split-K across the S ranks of the cluster: rank r owns tile rows
+// [r * R, (r + 1) * R). Every rank sends its FP32 partials of the rows it does
+// not own to their owner (st.async into the owner's exchange buffer,
+// red[q][row - r * R][t] for source rank q, counted on the owner's exchange
+// barrier); the owner adds q = 0, 1, ..., S-1 in that order, its own partial
+// taken from registers. A CTA leaves only after its exchange barrier has
+// counted every byte its peers send it, so no peer writes into shared memory
+// that is gone; one cluster barrier (before the first push) is enough.
+template <int NT, bool kScaled>
+__device__ __forceinline__ void splitk_store(const float (&acc)[kTokTile], float out_scale,
+                                             uint16_t *stage, float *red, uint32_t red_bar,
+                                             volatile uint32_t *abort_flag, bool aborted, int S,
+                                             int h, uint16_t *y, int n, int n0, int m) {
+  const int tid = threadIdx.x;
+  if (S == 1) {
+    float v[kTokTile];
+#pragma unroll
+    for (int t = 0; t < kTokTile; ++t) v[t] = kScaled ? __fmul_rn(acc[t], out_scale) : acc[t];
+    // Outputs may still be read or written by the previous kernel in the stream.
+    griddep_wait();
+    store_tile_rows<NT>(stage, v, 0, h, y, n, n0, m, !aborted);
+    return;
+  }
+  const int R = (h + S - 1) / S;
+  const uint32_t rank = cluster_ctarank();
+  const int lo = static_cast<int>(rank) * R;
+  const int hi = min(h, lo + R);
+  const int ng = (m + 3) / 4;  // groups of 4 tokens sent
+  if (tid == 0)
+    mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>((S - 1) * max(0, hi - lo) * ng * 16));
+  cluster_wait();  // every peer's exchange barrier is initialised
+  if (tid < h) {
+    const uint32_t owner = static_cast<uint32_t>(tid / R);
+    if (owner != rank) {
+      const int lr = tid - static_cast<int>(owner) * R;
+      const uint32_t dst =
+          dsmem_map(smem_u32(red + (static_cast<int>(rank) * R + lr) * kTokTile), owner);
+      const uint32_t rbar = dsmem_map(red_bar, owner);
+#pragma unroll
+      for (int g = 0; g < kTokTile / 4; ++g)
+        if (g < ng)
+          st_async_v4_f32(dst + 16 * g, acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3],
+                          rbar);
+    }
+  }
+  float v[kTokTile];
+  if (tid >= lo && tid < hi) {
+    if (!mbar_wait_bounded(red_bar, 0, kWaitLimitNs)) {
+      atomicOr(&g_device_status, SK_DEVICE_WAIT_EPILOGUE);
+      *abort_flag = 1;
+    }
+    // All sums first, then the stores: a load issued after a global store
+    // that the compiler cannot prove disjoint waits behind it.
+    const int lr = tid - lo;
+#pragma unroll
+    for (int t = 0; t < kTokTile; ++t) v[t] = acc[t];
+    if (rank != 0) {
+      const float4 *r0 = reinterpret_cast<const float4 *>(red + lr * kTokTile);
+#pragma unroll
+      for (int g = 0; g < kTokTile / 4; ++g) {
+        const float4 p = r0[g];
+        v[4 * g] = p.x;
+        v[4 * g + 1] = p.y;
+        v[4 * g + 2] = p.z;
+        v[4 * g + 3] = p.w;
+      }
+    }
+    for (int q = 1; q < S; ++q) {
+      if (q == static_cast<int>(rank)) {
+#pragma unroll
+        for (int t = 0; t < kTokTile; ++t) v[t] += acc[t];
+      } else {
+        const float4 *rq = reinterpret_cast<const float4 *>(red + (q * R + lr) * kTokTile);
+#pragma unroll
+        for (int g = 0; g < kTokTile / 4; ++g) {
+          const float4 p = rq[g];
+          v[4 * g] += p.x;
+          v[4 * g + 1] += p.y;
+          v[4 * g + 2] += p.z;
+          v[4 * g + 3] += p.w;
+        }
+      }
+    }
+    if (kScaled) {
+#pragma unroll
+      for (int t = 0; t < kTokTile; ++t) v[t] = __fmul_rn(v[t], out_scale);
+    }
+  }
+  __syncthreads();  // the exchange waits are over: *abort_flag is final
+  const bool ok = !*abort_flag;
+  // Outputs may still be read or written by the previous kernel in the
+  // stream (the exchange above stays within this cluster's shared memory).
+  griddep_wait();
+  if ((R & 7) == 0) {
+    store_tile_rows<NT>(stage, v, lo, hi > lo ? hi : lo, y, n, n0, m, ok);
+  } else if (ok && tid >= lo && tid < hi && n0 + tid < n) {
+#pragma unroll
+    for (int t = 0; t < kTokTile; ++t)
+      if (t < m) y[static_cast<size_t>(t) * n + n0 + tid] = bf16_store_bits(v[t]);
   }
 }
 
@@ -255,97 +365,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_sum_accumulators<kNumAcc>(tmem + (static_cast<uint32_t>(warp * 32) << 16),
                                    acc_used(nkb, B, kGemmIssuers), acc);
 
-  const int m = args.m, n = args.n;
-  uint16_t *y = args.y;
-  uint16_t *stage = reinterpret_cast<uint16_t *>(s_w);  // the ring is idle by now
-  if (args.splits == 1) {
-    // Outputs may still be read or written by the previous kernel in the stream.
-    griddep_wait();
-    store_tile_rows(stage, acc, 0, h, y, n, n0, m, !aborted);
-  } else {
-    // Split-K across the S ranks of the cluster. Rank r owns tile rows
-    // [r * R, (r + 1) * R). Every rank sends its FP32 partials of the rows it
-    // does not own to their owner (st.async into the owner's exchange buffer,
-    // red[q][row - r * R][t] for source rank q, counted on the owner's
-    // exchange barrier); the owner adds q = 0, 1, ..., S-1 in that order, its
-    // own partial taken from registers. A CTA leaves only after its exchange
-    // barrier has counted every byte its peers send it, so no peer writes into
-    // shared memory that is gone; one cluster barrier (before the first push)
-    // is enough.
-    const int R = (h + S - 1) / S;
-    const uint32_t rank = cluster_ctarank();
-    const int lo = static_cast<int>(rank) * R;
-    const int hi = min(h, lo + R);
-    const int ng = (m + 3) / 4;  // groups of 4 tokens sent
-    if (tid == 0)
-      mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>((S - 1) * max(0, hi - lo) * ng * 16));
-    cluster_wait();  // every peer's exchange barrier is initialised
-    if (tid < h) {
-      const uint32_t owner = static_cast<uint32_t>(tid / R);
-      if (owner != rank) {
-        const int lr = tid - static_cast<int>(owner) * R;
-        const uint32_t dst =
-            dsmem_map(smem_u32(red + (static_cast<int>(rank) * R + lr) * kTokTile), owner);
-        const uint32_t rbar = dsmem_map(red_bar, owner);
-#pragma unroll
-        for (int g = 0; g < kTokTile / 4; ++g)
-          if (g < ng)
-            st_async_v4_f32(dst + 16 * g, acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3],
-                            rbar);
-      }
-    }
-    float v[kTokTile];
-    if (tid >= lo && tid < hi) {
-      if (!mbar_wait_bounded(red_bar, 0, kWaitLimitNs)) {
-        atomicOr(&g_device_status, SK_DEVICE_WAIT_EPILOGUE);
-        *abort_flag = 1;
-      }
-      // All sums first, then the stores: a load issued after a global store
-      // that the compiler cannot prove disjoint waits behind it.
-      const int lr = tid - lo;
-#pragma unroll
-      for (int t = 0; t < kTokTile; ++t) v[t] = acc[t];
-      if (rank != 0) {
-        const float4 *r0 = reinterpret_cast<const float4 *>(red + lr * kTokTile);
-#pragma unroll
-        for (int g = 0; g < kTokTile / 4; ++g) {
-          const float4 p = r0[g];
-          v[4 * g] = p.x;
-          v[4 * g + 1] = p.y;
-          v[4 * g + 2] = p.z;
-          v[4 * g + 3] = p.w;
-        }
-      }
-      for (int q = 1; q < S; ++q) {
-        if (q == static_cast<int>(rank)) {
-#pragma unroll
-          for (int t = 0; t < kTokTile; ++t) v[t] += acc[t];
-        } else {
-          const float4 *rq = reinterpret_cast<const float4 *>(red + (q * R + lr) * kTokTile);
-#pragma unroll
-          for (int g = 0; g < kTokTile / 4; ++g) {
-            const float4 p = rq[g];
-            v[4 * g] += p.x;
-            v[4 * g + 1] += p.y;
-            v[4 * g + 2] += p.z;
-            v[4 * g + 3] += p.w;
-          }
-        }
-      }
-    }
-    __syncthreads();  // the exchange waits are over: *abort_flag is final
-    const bool ok = !*abort_flag;
-    // Outputs may still be read or written by the previous kernel in the
-    // stream (the exchange above stays within this cluster's shared memory).
-    griddep_wait();
-    if ((R & 7) == 0) {
-      store_tile_rows(stage, v, lo, hi > lo ? hi : lo, y, n, n0, m, ok);
-    } else if (ok && tid >= lo && tid < hi && n0 + tid < n) {
-#pragma unroll
-      for (int t = 0; t < kTokTile; ++t)
-        if (t < m) y[static_cast<size_t>(t) * n + n0 + tid] = bf16_store_bits(v[t]);
-    }
-  }
+  splitk_store<kGemmThreads, false>(acc, 1.0f, reinterpret_cast<uint16_t *>(s_w), red, red_bar,
+                                    abort_flag, aborted, S, h, args.y, args.n, n0, args.m);
 
   tc_fence_before_sync();
   __syncthreads();
@@ -357,6 +378,288 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Weight-only NVFP4 GEMM: y[m, n] = bf16(w_scale * sum_k x[m, k] * W[n, k])
+// with W held as e2m1 codes (two per byte, column 2c in the low nibble) and one
+// e4m3 scale per 16 columns of a row, the NVFP4 layout of the pooler page's
+// module docstring (cutedsl/moe/pooler_gather) applied to a weight. Not on the
+// pages: it streams 4.5 bits per weight instead of 16.
+//
+// Roles (kW4Threads threads): warp 0 lane 0 issues the copies (codes and
+// scales before the dependency wait, activations after it); lane 0 of warps
+// 1..kW4Issuers issue the MMAs (K-step t of a block goes to issuer t mod 4,
+// each with its own accumulator); warps kW4DeqWarp0.. expand the codes into a
+// BF16 operand in tensor memory and put each block's activations in the
+// order of that operand; warps 0-3 run the epilogue.
+//
+// Expansion. Placing an e2m1 code's three magnitude bits at bits 6..8 of a
+// BF16 word and its sign at bit 15 gives the code's value times 2^-126
+// (a subnormal for codes 1 and 9, whose exponent field is 0). One BF16 multiply
+// by the block scale times 2^119 (exact in BF16 for every e4m3 value) then
+// gives code * scale * 2^-7 exactly: at most six significant bits, within
+// [2^-17, 21]. The epilogue multiplies the FP32 sum by w_scale * 2^7.
+// Codes j and j + 4 of a 32-bit word (8 consecutive columns) sit 16 bits
+// apart, so one shift-and-mask yields the BF16 pair (W[j], W[j + 4]); the
+// operand therefore holds each group of 8 columns in the order
+// 0, 4, 1, 5, 2, 6, 3, 7, and the activations are permuted the same way in
+// shared memory (the dot product does not depend on the order of K).
+constexpr int kW4Issuers = 4;
+constexpr int kW4DeqWarp0 = 8;
+constexpr int kW4DeqWarps = 8;
+constexpr int kW4Threads = 32 * (kW4DeqWarp0 + kW4DeqWarps);
+constexpr int kW4TmemCols = 512;  // accumulators at 0, A buffers at 128, 256, 384
+static_assert(kW4ACols * (kW4ABufs + 1) <= kW4TmemCols, "tensor memory");
+static_assert(kW4Issuers * kTokTile <= kW4ACols, "accumulators overlap the A buffers");
+
+struct W4Args {
+  uint16_t *y;             // [m, n] BF16 bits
+  const float *w_scale;    // device FP32 [1]
+  int m, n;
+  int nblk;                // kW4BlockK-wide blocks per CTA (K slice)
+  int stages, splits, l2_ahead;
+};
+
+// BF16 pair (scale * 2^119, scale * 2^119) of an e4m3 block scale: exact.
+__device__ __forceinline__ uint32_t w4_scale_pair(uint32_t sf) {
+  const float f = __fmul_rn(cvt_e4m3_f32(sf), 0x1p119f);
+  return cvt_bf16x2(f, f);
+}
+
+// The four BF16 pairs (W[j], W[j + 4]), j = 0..3, of 8 codes (code j in bits
+// 4j..4j+3) times the scale pair c2, each an exact code * scale * 2^-7.
+__device__ __forceinline__ void w4_expand8(uint32_t w, uint32_t c2, uint32_t *o) {
+  o[0] = mul_bf16x2(((w << 6) & 0x01C001C0u) | ((w << 12) & 0x80008000u), c2);
+  o[1] = mul_bf16x2(((w << 2) & 0x01C001C0u) | ((w << 8) & 0x80008000u), c2);
+  o[2] = mul_bf16x2(((w >> 2) & 0x01C001C0u) | ((w << 4) & 0x80008000u), c2);
+  o[3] = mul_bf16x2(((w >> 6) & 0x01C001C0u) | (w & 0x80008000u), c2);
+}
+
+__global__ void __launch_bounds__(kW4Threads, 1)
+    gemm_nvfp4w_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                       const __grid_constant__ CUtensorMap tmap_sf,
+                       const __grid_constant__ CUtensorMap tmap_x, W4Args args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int stages = args.stages;
+  const int S = args.splits;
+  const W4Layout lay = w4_layout(stages, S);
+  uint8_t *s_q = smem;
+  uint8_t *s_x = smem + lay.x_off;
+  uint8_t *s_sf = smem + lay.sf_off;
+  float *red = reinterpret_cast<float *>(smem + lay.red_off);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * stages + 2 * kW4ABufs + 2);
+  volatile uint32_t *abort_flag = tmem_slot + 1;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n0 = blockIdx.x * kW4Rows;
+  const int nblk = args.nblk;
+  const int kb0 = blockIdx.y * nblk;
+  const uint32_t stage_tx = static_cast<uint32_t>(kW4StageBytes);
+
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + stages);
+  const uint32_t afull0 = smem_u32(bars + 2 * stages);
+  const uint32_t aempty0 = smem_u32(bars + 2 * stages + kW4ABufs);
+  const uint32_t done_bar = smem_u32(bars + 2 * stages + 2 * kW4ABufs);
+  const uint32_t red_bar = smem_u32(bars + 2 * stages + 2 * kW4ABufs + 1);
+
+  if (tid == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kW4Issuers);
+    }
+    for (int a = 0; a < kW4ABufs; ++a) {
+      mbar_init(afull0 + 8 * a, kW4DeqWarps);
+      mbar_init(aempty0 + 8 * a, kW4Issuers);
+    }
+    mbar_init(done_bar, kW4Issuers);
+    mbar_init(red_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_map(&tmap_q);
+    tma_prefetch_map(&tmap_sf);
+    tma_prefetch_map(&tmap_x);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), kW4TmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  if (S > 1) cluster_arrive();
+  griddep_launch_dependents();
+
+  int issued = 0;
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------- TMA producer
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_x = l2_policy_evict_last();
+    const int npre = nblk < stages ? nblk : stages;
+    for (int i = 0; i < npre; ++i) {
+      mbar_arrive_expect_tx(full0 + 8 * i, stage_tx);
+      tma_load_3d(smem_u32(s_q + i * kW4CodeBytes), &tmap_q, full0 + 8 * i, 0, n0, kb0 + i, pol_w);
+      tma_load_3d(smem_u32(s_sf + i * kW4ScaleBytes), &tmap_sf, full0 + 8 * i, 0, n0, kb0 + i,
+                  pol_w);
+    }
+    for (int i = npre; i < nblk && i < npre + args.l2_ahead; ++i) {
+      tma_prefetch_l2_3d(&tmap_q, 0, n0, kb0 + i);
+      tma_prefetch_l2_3d(&tmap_sf, 0, n0, kb0 + i);
+    }
+    griddep_wait();
+    for (int i = 0; i < npre; ++i)
+      tma_load_3d(smem_u32(s_x + i * kW4XBytes), &tmap_x, full0 + 8 * i, 0, 0, 4 * (kb0 + i),
+                  pol_x);
+    issued = npre;
+    for (int i = npre; i < nblk; ++i) {
+      const int s = i % stages;
+      if (!wait_or_abort(empty0 + 8 * s, ((i / stages) & 1) ^ 1, abort_flag)) {
+        atomicOr(&g_device_status, SK_DEVICE_WAIT_PRODUCER);
+        *abort_flag = 1;
+        break;
+      }
+      const uint32_t fb = full0 + 8 * s;
+      mbar_arrive_expect_tx(fb, stage_tx);
+      tma_load_3d(smem_u32(s_q + s * kW4CodeBytes), &tmap_q, fb, 0, n0, kb0 + i, pol_w);
+      tma_load_3d(smem_u32(s_sf + s * kW4ScaleBytes), &tmap_sf, fb, 0, n0, kb0 + i, pol_w);
+      tma_load_3d(smem_u32(s_x + s * kW4XBytes), &tmap_x, fb, 0, 0, 4 * (kb0 + i), pol_x);
+      issued = i + 1;
+    }
+  } else if (warp >= 1 && warp <= kW4Issuers && lane == 0) {
+    // ---------------------------------------------------- MMA issuers
+    const int q = warp - 1;
+    bool started = false;
+    for (int i = 0; i < nblk; ++i) {
+      const int s = i % stages, a = i % kW4ABufs;
+      if (!wait_or_abort(afull0 + 8 * a, (i / kW4ABufs) & 1, abort_flag)) {
+        atomicOr(&g_device_status, SK_DEVICE_WAIT_MMA);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t xs = smem_u32(s_x + s * kW4XBytes);
+      const uint32_t acol = static_cast<uint32_t>(kW4ACols * (a + 1));
+#pragma unroll
+      for (int t = q; t < kW4BlockK / 16; t += kW4Issuers) {
+        // K-step t: A columns acol + 8t; activations in 64-column box t / 4,
+        // 32 bytes further per K-step inside the 128-byte swizzled row
+        const uint64_t bdesc = smem_desc_k128(xs + (t / 4) * kSlotXBytes) + 2 * (t % 4);
+        tc_mma_bf16_tmem_a(tmem + static_cast<uint32_t>(q * kTokTile), tmem + acol + 8 * t, bdesc,
+                           kIdesc, started || t != q);
+      }
+      started = true;
+      tc_commit(aempty0 + 8 * a);  // the A buffer has been read
+      tc_commit(empty0 + 8 * s);   // and the stage's codes, scales and activations
+    }
+    tc_commit(done_bar);
+  } else if (warp >= kW4DeqWarp0) {
+    // ---------------------------------------------------- expansion
+    const int dw = warp - kW4DeqWarp0;
+    const int quad = warp & 3;        // TMEM lane quadrant this warp may access
+    const int hf = dw >> 2;           // K-steps 8 * hf .. 8 * hf + 7 of each block
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    for (int i = 0; i < nblk; ++i) {
+      const int s = i % stages, a = i % kW4ABufs;
+      if (!wait_or_abort(full0 + 8 * s, (i / stages) & 1, abort_flag)) {
+        atomicOr(&g_device_status, SK_DEVICE_WAIT_MMA);
+        *abort_flag = 1;
+        break;
+      }
+      if (i >= kW4ABufs &&
+          !wait_or_abort(aempty0 + 8 * a, ((i / kW4ABufs) - 1) & 1, abort_flag)) {
+        atomicOr(&g_device_status, SK_DEVICE_WAIT_MMA);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after_sync();
+      // the block's activations in operand order: each 16-byte chunk of 8
+      // columns x0..x7 becomes x0 x4 x1 x5 x2 x6 x3 x7 (chunks move whole
+      // under the 128-byte swizzle)
+      uint4 *xc = reinterpret_cast<uint4 *>(s_x + s * kW4XBytes);
+#pragma unroll
+      for (int c = dw * 32 + lane; c < kW4XBytes / 16; c += kW4DeqWarps * 32) {
+        const uint4 v = xc[c];
+        uint4 o;
+        o.x = __byte_perm(v.x, v.z, 0x5410);
+        o.y = __byte_perm(v.x, v.z, 0x7632);
+        o.z = __byte_perm(v.y, v.w, 0x5410);
+        o.w = __byte_perm(v.y, v.w, 0x7632);
+        xc[c] = o;
+      }
+      // this row's codes of K-steps 8hf..8hf+7: 64 bytes, four 16-byte chunks
+      // of its 128-byte swizzled row; its 8 scales
+      const uint8_t *qrow = s_q + s * kW4CodeBytes + row * 128;
+      const uint2 sc =
+          *reinterpret_cast<const uint2 *>(s_sf + s * kW4ScaleBytes + row * 16 + 8 * hf);
+      const uint32_t scw[2] = {sc.x, sc.y};
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {  // K-steps 8hf + 4part .. + 3
+        uint32_t o[32];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {     // one 16-byte chunk = 2 K-steps
+          const int chunk = 4 * hf + 2 * part + cc;
+          const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 16 * (chunk ^ (row & 7)));
+          const int ks = 2 * part + cc;        // K-step within this warp's 8, pair index
+          const uint32_t c0 = w4_scale_pair((scw[(2 * ks) >> 2] >> (8 * ((2 * ks) & 3))) & 0xFFu);
+          const uint32_t c1 =
+              w4_scale_pair((scw[(2 * ks + 1) >> 2] >> (8 * ((2 * ks + 1) & 3))) & 0xFFu);
+          w4_expand8(w.x, c0, o + 16 * cc);
+          w4_expand8(w.y, c0, o + 16 * cc + 4);
+          w4_expand8(w.z, c1, o + 16 * cc + 8);
+          w4_expand8(w.w, c1, o + 16 * cc + 12);
+        }
+        tmem_st_32x32b_x32(tmem + lane_base + kW4ACols * (a + 1) + 64 * hf + 32 * part, o);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();  // the permuted activations, for the MMAs
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(afull0 + 8 * a);
+    }
+  }
+  __syncwarp();
+
+  // ------------------------------------------------------------ epilogue
+  if (!mbar_wait_idle(done_bar, 0, kWaitLimitNs)) {
+    atomicOr(&g_device_status, SK_DEVICE_WAIT_EPILOGUE);
+    *abort_flag = 1;
+  }
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    const int first = issued > stages ? issued - stages : 0;
+    for (int j = first; j < issued; ++j)
+      mbar_wait_bounded(full0 + 8 * (j % stages), (j / stages) & 1, kWaitLimitNs);
+  }
+  __syncthreads();
+  const bool aborted = *abort_flag != 0;
+  tc_fence_after_sync();
+
+  float acc[kTokTile];
+#pragma unroll
+  for (int t = 0; t < kTokTile; ++t) acc[t] = 0.0f;
+  if (warp < 4 && !aborted)
+    tmem_sum_accumulators<kW4Issuers>(tmem + (static_cast<uint32_t>(warp * 32) << 16), kW4Issuers,
+                                      acc);
+  // w_scale may have been written by the kernel ahead in the stream
+  griddep_wait();
+  const float out_scale = __fmul_rn(*args.w_scale, 128.0f);
+  splitk_store<kW4Threads, true>(acc, out_scale, reinterpret_cast<uint16_t *>(s_q), red, red_bar,
+                                 abort_flag, aborted, S, kW4Rows, args.y, args.n, n0, args.m);
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 2) {
+    if (aborted && lane == 0 && !mbar_wait_idle(done_bar, 0, kWaitLimitNs))
+      atomicOr(&g_device_status, SK_DEVICE_WAIT_TEARDOWN);
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kW4TmemCols);
   }
 }
 
@@ -773,6 +1076,13 @@ cudaError_t device_setup(int device, DeviceInfo *info) {
         return e;
       if ((e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)))
         return e;
+      if ((e = cudaFuncGetAttributes(&fa, gemm_nvfp4w_kernel))) return e;
+      if ((e = cudaFuncSetAttribute(gemm_nvfp4w_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(d.max_smem_optin - fa.sharedSizeBytes))))
+        return e;
+      if ((e = cudaFuncSetAttribute(gemm_nvfp4w_kernel,
+                                    cudaFuncAttributeNonPortableClusterSizeAllowed, 1)))
+        return e;
     }
     g_info[device] = d;
     g_ready[device] = true;
@@ -862,6 +1172,59 @@ static void norm_shape(int units, int min_per_cta, int *C, int *threads) {
   const int per = (units + c - 1) / c;
   *C = c;
   *threads = (per + 31) / 32 * 32;
+}
+
+size_t w4_smem_bytes(int stages, int splits) {
+  const size_t b = 1024 + static_cast<size_t>(w4_layout(stages, splits).total);
+  return b < kW4MinSmem ? kW4MinSmem : b;
+}
+
+int w4_max_clusters(int device, int splits) {
+  static std::mutex mu;
+  static int cache[64][5];
+  int idx = 0;
+  while ((1 << idx) < splits && idx < 4) ++idx;
+  if (device < 0 || device >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[device][idx] == 0) {
+    int clusters = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, splits, 1);
+    cfg.blockDim = dim3(kW4Threads);
+    cfg.dynamicSmemBytes = w4_smem_bytes(kW4MaxStages, splits);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 1;
+    attr.val.clusterDim.y = static_cast<unsigned>(splits);
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_nvfp4w_kernel, &cfg) != cudaSuccess ||
+        clusters < 1)
+      clusters = -1;
+    cache[device][idx] = clusters;
+  }
+  return cache[device][idx];
+}
+
+cudaError_t launch_gemm_nvfp4w(const CUtensorMap &tmap_q, const CUtensorMap &tmap_sf,
+                               const CUtensorMap &tmap_x, const float *w_scale, uint16_t *y,
+                               int m, int n, int k, int splits, int stages, int l2_ahead,
+                               cudaStream_t stream, bool pdl) {
+  if (stages < 1 || stages > kW4MaxStages || splits < 1 || k % (kW4BlockK * splits))
+    return cudaErrorInvalidValue;
+  W4Args a = {};
+  a.y = y;
+  a.w_scale = w_scale;
+  a.m = m;
+  a.n = n;
+  a.nblk = k / (kW4BlockK * splits);
+  a.stages = stages < a.nblk ? stages : a.nblk;
+  a.splits = splits;
+  a.l2_ahead = l2_ahead < 0 ? 0 : (l2_ahead > 64 ? 64 : l2_ahead);
+  const dim3 grid((n + kW4Rows - 1) / kW4Rows, splits, 1);
+  return launch_ex(gemm_nvfp4w_kernel, grid, dim3(kW4Threads), w4_smem_bytes(a.stages, splits),
+                   stream, pdl, dim3(1, splits, 1), tmap_q, tmap_sf, tmap_x, a);
 }
 
 cudaError_t launch_rmsnorm_nvfp4(const uint16_t *y, const uint16_t *norm_w, float eps, float gc,

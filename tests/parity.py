@@ -57,17 +57,18 @@ GEMM_RECORDS: list = []
 
 
 def check_gemm(y_gpu_bits, y_ref_bits, acc, absacc, k: int, splits: int, max_frac_ii: float = 2e-4,
-               label: str | None = None):
+               label: str | None = None, gamma_extra: float = 0.0):
     """Asserts the GEMM tolerance; returns (n_strict_fail, n_total, max_ulp).
     n_strict_fail counts the outputs more than one BF16 ulp from the oracle's
     correctly rounded result, i.e. those accepted only by the cancellation
     clause (ii); with a ``label`` the counts are recorded for the session's
-    report."""
+    report. ``gamma_extra`` widens gamma for roundings after the sum (the
+    weight-only NVFP4 GEMM multiplies the FP32 sum by w_scale: 2^-24)."""
     y_gpu_bits = np.asarray(y_gpu_bits, np.uint16)
     d = ulp_distance(y_gpu_bits, y_ref_bits)
     strict = d <= 1
     g = bf16_to_f64(y_gpu_bits)
-    bound = 0.5 * bf16_ulp(g) + gemm_gamma(k, splits) * absacc
+    bound = 0.5 * bf16_ulp(g) + (gemm_gamma(k, splits) + gamma_extra) * absacc
     loose = np.abs(g - acc) <= bound
     bad = ~(strict | loose)
     if bad.any():

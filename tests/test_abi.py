@@ -145,3 +145,29 @@ def test_binding_raises_value_error_on_bad_tensors(sk):
     w = torch.zeros(128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         sk.gemm_bf16(x, w)
+
+
+@pytest.mark.parametrize("m,n,k,splits,status", [
+    (0, 128, 256, 0, 1), (17, 128, 256, 0, 1),        # m outside 1..16
+    (1, 24, 256, 0, 1),                                 # n not a multiple of 16
+    (1, 128, 128, 0, 1), (1, 128, 320, 0, 1),           # k not a multiple of 256
+    (1, 128, 256, 3, 2), (1, 128, 512, 4, 2),           # split count / uneven split
+])
+def test_nvfp4w_shape_validation(sk, m, n, k, splits, status):
+    lib = sk.lib()
+    vp = ctypes.c_void_p
+    assert lib.sk_gemm_nvfp4w_supported(m, n, k, splits) == status
+    assert sk.last_error()
+    st = lib.sk_gemm_nvfp4w_bf16(vp(P), vp(P), vp(P), vp(P), vp(P), m, n, k, splits, None)
+    assert st == status
+
+
+def test_nvfp4w_pointer_validation(sk):
+    lib = sk.lib()
+    vp = ctypes.c_void_p
+    assert lib.sk_gemm_nvfp4w_supported(16, 8192, 8192, 0) == 0
+    assert lib.sk_gemm_nvfp4w_bf16(vp(P), None, vp(P), vp(P), vp(P), 1, 128, 256, 0, None) == 1
+    assert lib.sk_gemm_nvfp4w_bf16(vp(P), vp(P), vp(P + 8), vp(P), vp(P), 1, 128, 256, 0, None) == 1
+    assert "aligned" in sk.last_error()
+    assert lib.sk_gemm_nvfp4w_bf16(vp(P), vp(P), vp(P), vp(P + 2), vp(P), 1, 128, 256, 0, None) == 1
+    assert "w_scale" in sk.last_error()
