@@ -328,7 +328,9 @@ def single_call_workloads(sk, synth, dev, stream, peak, min_calls: int = 200, co
       (N,K) in {(1024,4096),(8192,4096)} at the automatic split, plus every
       split count S in {1,2,4,8} at M=16;
     * the pooler GEMM [4096,8192] + RMSNorm + NVFP4 at b in {1,8,16};
-    * the o_proj GEMM [8192,1024] + dual norm at b in {1,4,16}.
+    * the o_proj GEMM [8192,1024] + dual norm at b in {1,4,16};
+    * the weight-only NVFP4 GEMM at M in {1,16} on [8192,8192], [4096,8192]
+      and [8192,4096] (bytes: codes, scales, activations and output).
     Automatic-split points also report `hinted_us_p50`: the same calls, each
     told the next call's weight (sk_gemm_prefetch_next)."""
     import torch
@@ -441,6 +443,30 @@ def single_call_workloads(sk, synth, dev, stream, peak, min_calls: int = 200, co
     sk.gemm_prefetch_next(None)
     del ws
     torch.cuda.empty_cache()
+
+    # weight-only NVFP4 GEMM: BF16 weights ~ N(0, 0.02) quantized on the device
+    # (sk_nvfp4_quantize, gs = 448 * 6 / amax), 4.5 bits per weight
+    for n, k in ((8192, 8192), (4096, 8192), (8192, 4096)):
+        wqs, wsfs, wss = [], [], []
+        for i in range(copies):
+            w = synth.normal_bf16((n, k), 0.02, 600 + i, device=dev)
+            gs_i = (2688.0 / w.float().abs().amax().clamp_min(1e-30)).reshape(1)
+            wq, wsf = sk.nvfp4_quantize(w, gs_i, stream=None)
+            wqs.append(wq)
+            wsfs.append(wsf)
+            wss.append((1.0 / gs_i).contiguous())
+            del w
+        torch.cuda.synchronize(dev)
+        for m in (1, 16):
+            x = synth.gemm_x(m, k).to(dev)
+            y = torch.empty(m, n, **bf)
+            per, nc = timed([lambda i=i: sk.gemm_nvfp4w(x, wqs[i], wsfs[i], wss[i], out=y, stream=stream)
+                             for i in range(copies)])
+            put(f"nvfp4w_m{m}_n{n}_k{k}", "weight-only NVFP4 GEMM", m, n, k,
+                f"auto({sk.gemm_nvfp4w_splits(m, n, k)})",
+                n * k // 2 + n * k // 16 + 4 + 2 * m * k + 2 * m * n, per, nc)
+        del wqs, wsfs, wss
+        torch.cuda.empty_cache()
     return out
 
 

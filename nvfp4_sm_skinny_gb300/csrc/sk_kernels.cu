@@ -393,7 +393,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // 1..kW4Issuers issue the MMAs (K-step t of a block goes to issuer t mod 4,
 // each with its own accumulator); warps kW4DeqWarp0.. expand the codes into a
 // BF16 operand in tensor memory and put each block's activations in the
-// order of that operand; warps 0-3 run the epilogue.
+// order of that operand, in two groups that take alternate blocks (one
+// group's barrier waits overlap the other's arithmetic); warps 0-3 run the
+// epilogue. Each MMA (128 weight rows x 16 tokens x 16) carries 2048 weights,
+// the same as in the BF16 GEMM, so the instruction count per SM is the same:
+// at 4.5 bits per weight the MMA issue rate of an SM (about one instruction
+// per 50 ns, whatever the number of issuing warps), not HBM, bounds this
+// kernel.
 //
 // Expansion. Placing an e2m1 code's three magnitude bits at bits 6..8 of a
 // BF16 word and its sign at bit 15 gives the code's value times 2^-126
@@ -408,11 +414,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // shared memory (the dot product does not depend on the order of K).
 constexpr int kW4Issuers = 4;
 constexpr int kW4DeqWarp0 = 8;
-constexpr int kW4DeqWarps = 8;
+constexpr int kW4DeqWarps = 16;
+// The expansion warps form kW4DeqGroups groups that take alternate blocks, so
+// that one group's barrier waits overlap another group's arithmetic. Within a
+// group the warps of a TMEM lane quadrant split the block's 16 K-steps.
+constexpr int kW4DeqGroups = 2;
+constexpr int kW4GroupWarps = kW4DeqWarps / kW4DeqGroups;
+constexpr int kW4StepsPerWarp = (kW4BlockK / 16) / (kW4GroupWarps / 4);
+static_assert(kW4StepsPerWarp % 4 == 0, "a warp stores whole groups of 4 K-steps");
 constexpr int kW4Threads = 32 * (kW4DeqWarp0 + kW4DeqWarps);
+static_assert(kW4Issuers < kW4DeqWarp0, "issuer warps 1..kW4Issuers precede the expansion warps");
 constexpr int kW4TmemCols = 512;  // accumulators at 0, A buffers at 128, 256, 384
 static_assert(kW4ACols * (kW4ABufs + 1) <= kW4TmemCols, "tensor memory");
 static_assert(kW4Issuers * kTokTile <= kW4ACols, "accumulators overlap the A buffers");
+static_assert(kW4XBytes % (16 * kW4GroupWarps * 32) == 0, "activation chunks per expansion thread");
 
 struct W4Args {
   uint16_t *y;             // [m, n] BF16 bits
@@ -422,19 +437,45 @@ struct W4Args {
   int stages, splits, l2_ahead;
 };
 
-// BF16 pair (scale * 2^119, scale * 2^119) of an e4m3 block scale: exact.
+// Bounded wait that also gives up once another role raised `abort`, for the
+// roles of this kernel that share their SM's issue slots with the expansion
+// warps: between polls the thread is suspended until the phase completes (or
+// the hint runs out) instead of issuing instructions.
+__device__ __forceinline__ bool w4_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_sleep(bar, parity, 200000u)) {
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// BF16 pair (scale * 2^119, scale * 2^119) of an e4m3 block scale, exact.
+// The byte's exponent and mantissa placed at bits 20..26 of an FP32 word give
+// |scale| * 2^-120 (an FP32 subnormal for subnormal scales); two exact
+// multiplies by 2^120 and 2^119 give |scale| * 2^119, whose low 16 bits are
+// zero (at most four significant bits), so its high half is the BF16 value.
+// The sign bit is copied into both halves.
 __device__ __forceinline__ uint32_t w4_scale_pair(uint32_t sf) {
-  const float f = __fmul_rn(cvt_e4m3_f32(sf), 0x1p119f);
-  return cvt_bf16x2(f, f);
+  const float mag = __uint_as_float((sf & 0x7Fu) * (1u << 20));
+  const uint32_t v = __float_as_uint(__fmul_rn(__fmul_rn(mag, 0x1p120f), 0x1p119f));
+  const uint32_t sign = (sf & 0x80u) * 0x01000100u;  // bit 7 -> bits 15 and 31
+  return __byte_perm(v, 0, 0x3232) | sign;
 }
 
 // The four BF16 pairs (W[j], W[j + 4]), j = 0..3, of 8 codes (code j in bits
-// 4j..4j+3) times the scale pair c2, each an exact code * scale * 2^-7.
+// 4j..4j+3) times the scale pair c2, each an exact code * scale * 2^-7. Codes
+// j and j + 4 sit 16 bits apart, so one left shift places both magnitudes at
+// bits 6..8 / 22..24 and another both signs at bits 15 / 31; the shifts are
+// written as multiplies (they run on the multiply-add pipe, beside the
+// logic operations), codes 2, 3, 6, 7 after one right shift of the word.
 __device__ __forceinline__ void w4_expand8(uint32_t w, uint32_t c2, uint32_t *o) {
-  o[0] = mul_bf16x2(((w << 6) & 0x01C001C0u) | ((w << 12) & 0x80008000u), c2);
-  o[1] = mul_bf16x2(((w << 2) & 0x01C001C0u) | ((w << 8) & 0x80008000u), c2);
-  o[2] = mul_bf16x2(((w >> 2) & 0x01C001C0u) | ((w << 4) & 0x80008000u), c2);
-  o[3] = mul_bf16x2(((w >> 6) & 0x01C001C0u) | (w & 0x80008000u), c2);
+  const uint32_t h = w >> 8;
+  o[0] = mul_bf16x2(((w * 64u) & 0x01C001C0u) | ((w * 4096u) & 0x80008000u), c2);
+  o[1] = mul_bf16x2(((w * 4u) & 0x01C001C0u) | ((w * 256u) & 0x80008000u), c2);
+  o[2] = mul_bf16x2(((h * 64u) & 0x01C001C0u) | ((h * 4096u) & 0x80008000u), c2);
+  o[3] = mul_bf16x2(((h * 4u) & 0x01C001C0u) | ((h * 256u) & 0x80008000u), c2);
 }
 
 __global__ void __launch_bounds__(kW4Threads, 1)
@@ -474,7 +515,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       mbar_init(empty0 + 8 * s, kW4Issuers);
     }
     for (int a = 0; a < kW4ABufs; ++a) {
-      mbar_init(afull0 + 8 * a, kW4DeqWarps);
+      mbar_init(afull0 + 8 * a, kW4GroupWarps);
       mbar_init(aempty0 + 8 * a, kW4Issuers);
     }
     mbar_init(done_bar, kW4Issuers);
@@ -519,7 +560,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     issued = npre;
     for (int i = npre; i < nblk; ++i) {
       const int s = i % stages;
-      if (!wait_or_abort(empty0 + 8 * s, ((i / stages) & 1) ^ 1, abort_flag)) {
+      if (!w4_wait(empty0 + 8 * s, ((i / stages) & 1) ^ 1, abort_flag)) {
         atomicOr(&g_device_status, SK_DEVICE_WAIT_PRODUCER);
         *abort_flag = 1;
         break;
@@ -537,7 +578,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     bool started = false;
     for (int i = 0; i < nblk; ++i) {
       const int s = i % stages, a = i % kW4ABufs;
-      if (!wait_or_abort(afull0 + 8 * a, (i / kW4ABufs) & 1, abort_flag)) {
+      if (!w4_wait(afull0 + 8 * a, (i / kW4ABufs) & 1, abort_flag)) {
         atomicOr(&g_device_status, SK_DEVICE_WAIT_MMA);
         *abort_flag = 1;
         break;
@@ -558,64 +599,76 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       tc_commit(empty0 + 8 * s);   // and the stage's codes, scales and activations
     }
     tc_commit(done_bar);
-  } else if (warp >= kW4DeqWarp0) {
-    // ---------------------------------------------------- expansion
+  } else if (warp >= kW4DeqWarp0 && warp < kW4DeqWarp0 + kW4DeqWarps) {
+    // ---------------------------------------------------- expansion (whole warps)
     const int dw = warp - kW4DeqWarp0;
-    const int quad = warp & 3;        // TMEM lane quadrant this warp may access
-    const int hf = dw >> 2;           // K-steps 8 * hf .. 8 * hf + 7 of each block
+    const int grp = dw / kW4GroupWarps;   // blocks grp, grp + kW4DeqGroups, ...
+    const int gw = dw % kW4GroupWarps;    // warp within the group
+    const int quad = warp & 3;            // TMEM lane quadrant this warp may access
+    const int part = gw >> 2;             // K-steps part * kW4StepsPerWarp .. of each block
     const int row = quad * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    for (int i = 0; i < nblk; ++i) {
+    constexpr int kChunks = kW4StepsPerWarp / 2;  // 16-byte code chunks (2 K-steps each)
+    constexpr int kXChunks = kW4XBytes / 16 / (kW4GroupWarps * 32);
+    for (int i = grp; i < nblk; i += kW4DeqGroups) {
       const int s = i % stages, a = i % kW4ABufs;
-      if (!wait_or_abort(full0 + 8 * s, (i / stages) & 1, abort_flag)) {
+      if (!w4_wait(full0 + 8 * s, (i / stages) & 1, abort_flag)) {
         atomicOr(&g_device_status, SK_DEVICE_WAIT_MMA);
         *abort_flag = 1;
         break;
       }
       if (i >= kW4ABufs &&
-          !wait_or_abort(aempty0 + 8 * a, ((i / kW4ABufs) - 1) & 1, abort_flag)) {
+          !w4_wait(aempty0 + 8 * a, ((i / kW4ABufs) - 1) & 1, abort_flag)) {
         atomicOr(&g_device_status, SK_DEVICE_WAIT_MMA);
         *abort_flag = 1;
         break;
       }
       tc_fence_after_sync();
+      // Loads first: this row's codes of this warp's K-steps (16-byte chunks
+      // of its 128-byte swizzled row), their scales, and this thread's share
+      // of the block's activations.
+      const uint32_t qrow = smem_u32(s_q + s * kW4CodeBytes) + row * 128;
+      uint4 w[kChunks];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c)
+        w[c] = lds128(qrow + 16 * ((kChunks * part + c) ^ (row & 7)));
+      uint32_t scw[kW4StepsPerWarp / 4];
+#pragma unroll
+      for (int j = 0; j < kW4StepsPerWarp / 4; ++j)
+        scw[j] = lds32(smem_u32(s_sf + s * kW4ScaleBytes) + row * 16 + kW4StepsPerWarp * part + 4 * j);
+      const uint32_t xs = smem_u32(s_x + s * kW4XBytes);
+      uint4 xv[kXChunks];
+#pragma unroll
+      for (int j = 0; j < kXChunks; ++j)
+        xv[j] = lds128(xs + 16 * (gw * 32 + lane + j * kW4GroupWarps * 32));
       // the block's activations in operand order: each 16-byte chunk of 8
       // columns x0..x7 becomes x0 x4 x1 x5 x2 x6 x3 x7 (chunks move whole
       // under the 128-byte swizzle)
-      uint4 *xc = reinterpret_cast<uint4 *>(s_x + s * kW4XBytes);
 #pragma unroll
-      for (int c = dw * 32 + lane; c < kW4XBytes / 16; c += kW4DeqWarps * 32) {
-        const uint4 v = xc[c];
+      for (int j = 0; j < kXChunks; ++j) {
         uint4 o;
-        o.x = __byte_perm(v.x, v.z, 0x5410);
-        o.y = __byte_perm(v.x, v.z, 0x7632);
-        o.z = __byte_perm(v.y, v.w, 0x5410);
-        o.w = __byte_perm(v.y, v.w, 0x7632);
-        xc[c] = o;
+        o.x = __byte_perm(xv[j].x, xv[j].z, 0x5410);
+        o.y = __byte_perm(xv[j].x, xv[j].z, 0x7632);
+        o.z = __byte_perm(xv[j].y, xv[j].w, 0x5410);
+        o.w = __byte_perm(xv[j].y, xv[j].w, 0x7632);
+        sts128(xs + 16 * (gw * 32 + lane + j * kW4GroupWarps * 32), o);
       }
-      // this row's codes of K-steps 8hf..8hf+7: 64 bytes, four 16-byte chunks
-      // of its 128-byte swizzled row; its 8 scales
-      const uint8_t *qrow = s_q + s * kW4CodeBytes + row * 128;
-      const uint2 sc =
-          *reinterpret_cast<const uint2 *>(s_sf + s * kW4ScaleBytes + row * 16 + 8 * hf);
-      const uint32_t scw[2] = {sc.x, sc.y};
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {  // K-steps 8hf + 4part .. + 3
+      for (int g = 0; g < kW4StepsPerWarp / 4; ++g) {  // groups of 4 K-steps
         uint32_t o[32];
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {     // one 16-byte chunk = 2 K-steps
-          const int chunk = 4 * hf + 2 * part + cc;
-          const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 16 * (chunk ^ (row & 7)));
-          const int ks = 2 * part + cc;        // K-step within this warp's 8, pair index
-          const uint32_t c0 = w4_scale_pair((scw[(2 * ks) >> 2] >> (8 * ((2 * ks) & 3))) & 0xFFu);
-          const uint32_t c1 =
-              w4_scale_pair((scw[(2 * ks + 1) >> 2] >> (8 * ((2 * ks + 1) & 3))) & 0xFFu);
-          w4_expand8(w.x, c0, o + 16 * cc);
-          w4_expand8(w.y, c0, o + 16 * cc + 4);
-          w4_expand8(w.z, c1, o + 16 * cc + 8);
-          w4_expand8(w.w, c1, o + 16 * cc + 12);
+        for (int cc = 0; cc < 2; ++cc) {              // one 16-byte chunk = 2 K-steps
+          const uint4 wc = w[2 * g + cc];
+          const uint32_t c0 = w4_scale_pair((scw[g] >> (16 * cc)) & 0xFFu);
+          const uint32_t c1 = w4_scale_pair((scw[g] >> (16 * cc + 8)) & 0xFFu);
+          w4_expand8(wc.x, c0, o + 16 * cc);
+          w4_expand8(wc.y, c0, o + 16 * cc + 4);
+          w4_expand8(wc.z, c1, o + 16 * cc + 8);
+          w4_expand8(wc.w, c1, o + 16 * cc + 12);
         }
-        tmem_st_32x32b_x32(tmem + lane_base + kW4ACols * (a + 1) + 64 * hf + 32 * part, o);
+        tmem_st_32x32b_x32(tmem + lane_base + kW4ACols * (a + 1) +
+                               8 * (kW4StepsPerWarp * part + 4 * g),
+                           o);
       }
       tmem_st_wait();
       fence_proxy_async_smem();  // the permuted activations, for the MMAs
@@ -1220,6 +1273,11 @@ cudaError_t launch_gemm_nvfp4w(const CUtensorMap &tmap_q, const CUtensorMap &tma
   a.n = n;
   a.nblk = k / (kW4BlockK * splits);
   a.stages = stages < a.nblk ? stages : a.nblk;
+  // A ring slot reused within the slice must be consumed by one expansion
+  // group only (blocks alternate between the groups), so that every wait on
+  // its barrier is for the next phase: an even number of stages.
+  if (a.stages < a.nblk && a.stages % kW4DeqGroups) a.stages -= a.stages % kW4DeqGroups;
+  if (a.stages < kW4DeqGroups && a.nblk > a.stages) a.stages = kW4DeqGroups;
   a.splits = splits;
   a.l2_ahead = l2_ahead < 0 ? 0 : (l2_ahead > 64 ? 64 : l2_ahead);
   const dim3 grid((n + kW4Rows - 1) / kW4Rows, splits, 1);
