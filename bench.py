@@ -318,7 +318,8 @@ def quantiles(xs, qs=(0.1, 0.5, 0.9)):
     return out
 
 
-def single_call_workloads(sk, synth, dev, stream, peak, min_calls: int = 200, copies: int = 48):
+def single_call_workloads(sk, synth, dev, stream, peak, min_calls: int = 200, copies: int = 48,
+                          only: str | None = None):
     """Per-call timings of the single-call workloads, each point a CUDA graph of
     one call per weight copy (48 copies, more bytes than L2), replayed until at
     least `min_calls` calls are timed: µs per call as median, p10 and p90 over
@@ -332,7 +333,10 @@ def single_call_workloads(sk, synth, dev, stream, peak, min_calls: int = 200, co
     * the weight-only NVFP4 GEMM at M in {1,16} on [8192,8192], [4096,8192]
       and [8192,4096] (bytes: codes, scales, activations and output).
     Automatic-split points also report `hinted_us_p50`: the same calls, each
-    told the next call's weight (sk_gemm_prefetch_next)."""
+    told the next call's weight (sk_gemm_prefetch_next); GEMM points also
+    `x_ready_us_p50`: hinted calls on an input no kernel writes
+    (sk_gemm_bf16_ex, SK_GEMM_X_READY), which overlap call with call. `only`
+    (a substring of the point names) restricts the run to matching points."""
     import torch
 
     bf = dict(dtype=torch.bfloat16, device=dev)
@@ -363,7 +367,10 @@ def single_call_workloads(sk, synth, dev, stream, peak, min_calls: int = 200, co
             return f
         return [one(i) for i in range(len(ws))]
 
-    def put(key, workload, m, n, k, splits, nbytes, per, ncalls, hint_per=None):
+    def want(key):
+        return only is None or only in key
+
+    def put(key, workload, m, n, k, splits, nbytes, per, ncalls, hint_per=None, xr_per=None):
         p10, p50, p90 = quantiles(per)
         gbs = nbytes / p50 / 1e9
         r = {"workload": workload, "m": m, "n": n, "k": k, "splits": splits,
@@ -374,19 +381,32 @@ def single_call_workloads(sk, synth, dev, stream, peak, min_calls: int = 200, co
             h50 = quantiles(hint_per, (0.5,))[0]
             r["hinted_us_p50"] = round(h50 * 1e6, 3)
             r["hinted_pct_of_peak"] = round(100.0 * nbytes / h50 / 1e9 / peak, 2)
+        if xr_per is not None:
+            x50 = quantiles(xr_per, (0.5,))[0]
+            r["x_ready_us_p50"] = round(x50 * 1e6, 3)
+            r["x_ready_pct_of_peak"] = round(100.0 * nbytes / x50 / 1e9 / peak, 2)
         out[key] = r
 
     for n, k in ((1024, 4096), (8192, 4096)):
+        if not any(want(f"gemm_m{m}_n{n}_k{k}") for m in (1, 2, 4, 8, 16)):
+            continue
         ws = [synth.gemm_weight(n, k, i, device=dev) for i in range(copies)]
         for m in (1, 2, 4, 8, 16):
+            if not want(f"gemm_m{m}_n{n}_k{k}"):
+                continue
             x = synth.gemm_x(m, k).to(dev)
             y = torch.empty(m, n, **bf)
             nbytes = 2 * n * k + 2 * m * k + 2 * m * n
             per, nc = timed([lambda w=w: sk.gemm_bf16(x, w, out=y, stream=stream) for w in ws])
             hper, _ = timed(hinted(ws, lambda w: sk.gemm_bf16(x, w, out=y, stream=stream)))
+            # x is written by no kernel here (one host copy, synchronised): the
+            # calls may read it without waiting for the call ahead of them
+            torch.cuda.synchronize(dev)
+            xper, _ = timed(hinted(ws, lambda w: sk.gemm_bf16(x, w, out=y, stream=stream,
+                                                              x_ready=True)))
             wl = "unpooler GEMM" if m == 1 and n == 1024 else "GEMM"
             put(f"gemm_m{m}_n{n}_k{k}", wl, m, n, k, f"auto({sk.gemm_splits(m, n, k)})", nbytes,
-                per, nc, hper)
+                per, nc, hper, xper)
             if m == 16:
                 for S in (1, 2, 4, 8):
                     if sk.gemm_supported(m, n, k, S) is not None:
@@ -399,10 +419,11 @@ def single_call_workloads(sk, synth, dev, stream, peak, min_calls: int = 200, co
         torch.cuda.empty_cache()
 
     H, P = synth.HIDDEN, synth.POOLED
-    ws = [synth.normal_bf16((P, H), 0.02, 200 + i, device=dev) for i in range(copies)]
+    pool_b = [b for b in (1, 8, 16) if want(f"pooler_nvfp4_b{b}")]
+    ws = [synth.normal_bf16((P, H), 0.02, 200 + i, device=dev) for i in range(copies)] if pool_b else []
     nw = synth.normal_bf16((P,), 0.1, 300, device=dev)
     gs = torch.tensor([300.0], dtype=torch.float32, device=dev)
-    for b in (1, 8, 16):
+    for b in pool_b:
         x = synth.normal_bf16((b, H), 1.0, 0, device=dev)
         a = torch.empty(b, P // 2, dtype=torch.uint8, device=dev)
         a_sf = torch.empty(b, P // 16, dtype=torch.uint8, device=dev)
@@ -421,11 +442,12 @@ def single_call_workloads(sk, synth, dev, stream, peak, min_calls: int = 200, co
     torch.cuda.empty_cache()
 
     K = synth.OPROJ_K
-    ws = [synth.normal_bf16((H, K), 0.02, 400 + i, device=dev) for i in range(copies)]
+    dual_b = [b for b in (1, 4, 16) if want(f"oproj_dual_b{b}")]
+    ws = [synth.normal_bf16((H, K), 0.02, 400 + i, device=dev) for i in range(copies)] if dual_b else []
     post_w = synth.normal_bf16((H,), 0.1, 500, mean=1.0, device=dev)
     pre_w = synth.normal_bf16((H,), 0.1, 501, mean=1.0, device=dev)
     beta = synth.uniform_bf16((H,), 0.5, 1.5, 502, device=dev)
-    for b in (1, 4, 16):
+    for b in dual_b:
         x = synth.normal_bf16((b, K), 1.0, 0, device=dev)
         # the residual stream is updated in place and drifts from call to call
         s_res = synth.normal_f32((b, H), 503, device=dev)
@@ -447,6 +469,8 @@ def single_call_workloads(sk, synth, dev, stream, peak, min_calls: int = 200, co
     # weight-only NVFP4 GEMM: BF16 weights ~ N(0, 0.02) quantized on the device
     # (sk_nvfp4_quantize, gs = 448 * 6 / amax), 4.5 bits per weight
     for n, k in ((8192, 8192), (4096, 8192), (8192, 4096)):
+        if not any(want(f"nvfp4w_m{m}_n{n}_k{k}") for m in (1, 16)):
+            continue
         wqs, wsfs, wss = [], [], []
         for i in range(copies):
             w = synth.normal_bf16((n, k), 0.02, 600 + i, device=dev)
@@ -458,6 +482,8 @@ def single_call_workloads(sk, synth, dev, stream, peak, min_calls: int = 200, co
             del w
         torch.cuda.synchronize(dev)
         for m in (1, 16):
+            if not want(f"nvfp4w_m{m}_n{n}_k{k}"):
+                continue
             x = synth.gemm_x(m, k).to(dev)
             y = torch.empty(m, n, **bf)
             per, nc = timed([lambda i=i: sk.gemm_nvfp4w(x, wqs[i], wsfs[i], wss[i], out=y, stream=stream)
@@ -648,12 +674,9 @@ def run_gpu(args, world, rank, local):
 
 # ---------------------------------------------------------------- sweep ----
 def run_sweep(args, local):
-    """Per-call timings of the single-call workloads (GEMM at M = 1..16 and
-    every split count, pooler + RMSNorm + NVFP4, o_proj + dual norm): each
-    point is a CUDA graph of one call per weight copy (48 copies drawn on the
-    device, more bytes than L2), replayed after warm-up; µs/call, algorithmic
-    GB/s and % of the HBM peak. One JSON line per point, then a markdown
-    table."""
+    """The single-call workloads of the default run's per_config, alone: one
+    JSON line per point, then a markdown table. --only restricts the points
+    (a substring of their names, e.g. nvfp4w_m16_n8192_k8192)."""
     import torch
 
     from __graft_entry__ import build
@@ -665,118 +688,16 @@ def run_sweep(args, local):
     dev = torch.device("cuda", local)
     peak, peak_src = hbm_peak()
     stream = torch.cuda.Stream(dev)
-    copies = 48
-    bf = dict(dtype=torch.bfloat16, device=dev)
-    rows = []
-
-    def per_call(calls, min_calls=200):
-        with torch.cuda.stream(stream):
-            for c in calls:
-                c()
-        torch.cuda.synchronize(dev)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for c in calls:
-                c()
-        for _ in range(3):
-            with torch.cuda.stream(stream):
-                g.replay()
-        reps = max(3, -(-min_calls // len(calls)))
-        best = min(time_graph(g, reps, stream) for _ in range(3))
-        return best / (reps * len(calls))
-
-    def record(workload, m, n, k, splits, sec, nbytes):
-        gbs = nbytes / sec / 1e9
-        r = dict(workload=workload, m=m, n=n, k=k, splits=splits, us_per_call=round(sec * 1e6, 3),
-                 gbs=round(gbs, 1), pct_of_peak=round(100 * gbs / peak, 1), bytes=nbytes)
-        rows.append(r)
-        print(json.dumps(r), flush=True)
-
-    def hinted(ws, call):
-        """The same calls, each told the next call's weight (sk_gemm_prefetch_next;
-        the last one the first's, for the next replay)."""
-        def one(i):
-            def f():
-                sk.gemm_prefetch_next(ws[(i + 1) % len(ws)])
-                call(ws[i])
-            return f
-        return [one(i) for i in range(len(ws))]
-
-    # GEMM (the unpooler shard and the sweep)
-    for n, k in ((1024, 4096), (8192, 4096)):
-        ws = [synth.gemm_weight(n, k, i, device=dev) for i in range(copies)]
-        for m in (1, 2, 4, 8, 16):
-            x = synth.gemm_x(m, k).to(dev)
-            y = torch.empty(m, n, **bf)
-            for S in (0, 1, 2, 4, 8):
-                if sk.gemm_supported(m, n, k, S) is not None:
-                    continue
-                sec = per_call([lambda w=w, S=S: sk.gemm_bf16(x, w, out=y, splits=S, stream=stream)
-                                for w in ws])
-                record("gemm", m, n, k, S if S else f"auto({sk.gemm_splits(m, n, k)})", sec,
-                       2 * n * k + 2 * m * k + 2 * m * n)
-            sec = per_call(hinted(ws, lambda w: sk.gemm_bf16(x, w, out=y, stream=stream)))
-            record("gemm, next weight hinted", m, n, k, f"auto({sk.gemm_splits(m, n, k)})", sec,
-                   2 * n * k + 2 * m * k + 2 * m * n)
-            # x is written by no kernel here (one host copy, synchronised): the
-            # calls may read it without waiting for the call ahead of them
-            torch.cuda.synchronize(dev)
-            sec = per_call(hinted(ws, lambda w: sk.gemm_bf16(x, w, out=y, stream=stream,
-                                                             x_ready=True)))
-            record("gemm, x ready, next weight hinted", m, n, k,
-                   f"auto({sk.gemm_splits(m, n, k)})", sec, 2 * n * k + 2 * m * k + 2 * m * n)
-        del ws
-        torch.cuda.empty_cache()
-    # pooler GEMM + pre-expert RMSNorm + NVFP4
-    H, P = synth.HIDDEN, synth.POOLED
-    ws = [synth.normal_bf16((P, H), 0.02, 200 + i, device=dev) for i in range(copies)]
-    nw = synth.normal_bf16((P,), 0.1, 300, device=dev)
-    gs = torch.tensor([300.0], dtype=torch.float32, device=dev)
-    for b in (1, 8, 16):
-        x = synth.normal_bf16((b, H), 1.0, 0, device=dev)
-        a = torch.empty(b, P // 2, dtype=torch.uint8, device=dev)
-        a_sf = torch.empty(b, P // 16, dtype=torch.uint8, device=dev)
-        wsp = torch.empty(sk.gemm_rmsnorm_nvfp4_workspace(b, P), dtype=torch.uint8, device=dev)
-        sec = per_call([lambda w=w: sk.gemm_rmsnorm_nvfp4(x, w, nw, synth.EPS, synth.GAIN_CENTER, gs,
-                                                          a=a, a_sf=a_sf, workspace=wsp, stream=stream)
-                        for w in ws])
-        record("pooler+rmsnorm+nvfp4", b, P, H, f"auto({sk.gemm_splits(b, P, H)})", sec,
-               2 * P * H + 2 * b * H + 2 * P + 4 + b * P // 2 + b * P // 16)
-        sec = per_call(hinted(ws, lambda w: sk.gemm_rmsnorm_nvfp4(
-            x, w, nw, synth.EPS, synth.GAIN_CENTER, gs, a=a, a_sf=a_sf, workspace=wsp, stream=stream)))
-        record("pooler+rmsnorm+nvfp4, next weight hinted", b, P, H,
-               f"auto({sk.gemm_splits(b, P, H)})", sec,
-               2 * P * H + 2 * b * H + 2 * P + 4 + b * P // 2 + b * P // 16)
-    del ws
-    torch.cuda.empty_cache()
-    # o_proj GEMM + dual norm (the residual stream drifts from call to call)
-    K = synth.OPROJ_K
-    ws = [synth.normal_bf16((H, K), 0.02, 400 + i, device=dev) for i in range(copies)]
-    post_w = synth.normal_bf16((H,), 0.1, 500, mean=1.0, device=dev)
-    pre_w = synth.normal_bf16((H,), 0.1, 501, mean=1.0, device=dev)
-    beta = synth.uniform_bf16((H,), 0.5, 1.5, 502, device=dev)
-    for b in (1, 4, 16):
-        x = synth.normal_bf16((b, K), 1.0, 0, device=dev)
-        s_res = synth.normal_f32((b, H), 503, device=dev)
-        out = torch.empty(b, H, **bf)
-        wsp = torch.empty(sk.gemm_dual_norm_workspace(b, H), dtype=torch.uint8, device=dev)
-        sec = per_call([lambda w=w: sk.gemm_dual_norm(x, w, s_res, post_w, 1.0, beta, pre_w, out=out,
-                                                      eps_post=synth.EPS, eps_pre=synth.EPS,
-                                                      workspace=wsp, stream=stream)
-                        for w in ws])
-        record("oproj+dual_norm", b, H, K, f"auto({sk.gemm_splits(b, H, K)})", sec,
-               2 * H * K + 2 * b * K + 3 * 2 * H + 2 * 4 * b * H + 2 * b * H)
-        sec = per_call(hinted(ws, lambda w: sk.gemm_dual_norm(
-            x, w, s_res, post_w, 1.0, beta, pre_w, out=out, eps_post=synth.EPS, eps_pre=synth.EPS,
-            workspace=wsp, stream=stream)))
-        record("oproj+dual_norm, next weight hinted", b, H, K, f"auto({sk.gemm_splits(b, H, K)})",
-               sec, 2 * H * K + 2 * b * K + 3 * 2 * H + 2 * 4 * b * H + 2 * b * H)
-    sk.gemm_prefetch_next(None)
-    print(f"\n| workload | M | N | K | splits | µs/call | GB/s | % of {peak_src} peak ({peak:.0f} GB/s) |")
-    print("|---|---|---|---|---|---|---|---|")
-    for r in rows:
-        print(f"| {r['workload']} | {r['m']} | {r['n']} | {r['k']} | {r['splits']} | "
-              f"{r['us_per_call']:.2f} | {r['gbs']:.0f} | {r['pct_of_peak']:.1f} |")
+    rows = single_call_workloads(sk, synth, dev, stream, peak, only=args.only)
+    for key, r in rows.items():
+        print(json.dumps(dict(point=key, **r)), flush=True)
+    print(f"\n| point | workload | M | N | K | splits | µs/call p50 (p10-p90) | GB/s | % of {peak_src} "
+          f"peak ({peak:.0f} GB/s) | hinted µs | x ready µs |")
+    print("|---|---|---|---|---|---|---|---|---|---|---|")
+    for key, r in rows.items():
+        print(f"| {key} | {r['workload']} | {r['m']} | {r['n']} | {r['k']} | {r['splits']} | "
+              f"{r['us_p50']:.2f} ({r['us_p10']:.2f}-{r['us_p90']:.2f}) | {r['gbs']:.0f} | "
+              f"{r['pct_of_peak']:.1f} | {r.get('hinted_us_p50', '')} | {r.get('x_ready_us_p50', '')} |")
     print(f"\ndevice status {sk.device_status()}")
     return 0
 
@@ -795,6 +716,8 @@ def main(argv=None):
                     help="chain depth (48 is the benchmark; fewer only for small profiling runs)")
     ap.add_argument("--sweep", action="store_true",
                     help="per-call timings of the single-call workloads instead of the chain")
+    ap.add_argument("--only", default=None,
+                    help="with --sweep: only the points whose names contain this string")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
