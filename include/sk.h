@@ -17,9 +17,10 @@
  *   - The caller owns every buffer. No call allocates device or host memory,
  *     no call synchronizes, and no call compiles anything: each one only
  *     validates its arguments on the host and enqueues kernels on `stream`
- *     (a cudaStream_t; NULL is the legacy default stream). The calls can be
- *     captured into a CUDA graph once the device has been used by the library
- *     (first call does one-time per-device set-up of kernel attributes).
+ *     (a cudaStream_t; NULL is the legacy default stream). The calls other
+ *     than sk_gemm_rmsnorm_nvfp4_static can be captured into a CUDA graph once
+ *     the device has been used by the library (first call does one-time
+ *     per-device set-up of kernel attributes).
  *   - Kernels are chained with programmatic dependent launch: weights (which
  *     no kernel writes) are read before a kernel waits for its predecessor in
  *     the stream; activations are read, and outputs written, only after it.
@@ -291,9 +292,8 @@ int sk_gemm_nvfp4w_splits(int m, int n, int k, int splits);
 /*
  * sk_gemm_rmsnorm_nvfp4_static -- sk_gemm_rmsnorm_nvfp4 without a workspace
  * argument, for callers that cannot allocate device memory: an inference-
- * engine plugin whose enqueue function is handed no workspace, code that is
- * being recorded into a CUDA graph (cudaMalloc cannot be captured), or a
- * serving loop whose memory is budgeted once at start-up. The pages have no
+ * engine plugin whose enqueue function is handed no workspace, or a serving
+ * loop whose memory is budgeted once at start-up. The pages have no
  * counterpart to this call; it is an addition of this library.
  *   Same arguments, results and constraints as sk_gemm_rmsnorm_nvfp4, less
  *   workspace/workspace_bytes, plus m * n <= SK_STATIC_SCRATCH_BYTES / 2:
@@ -302,10 +302,9 @@ int sk_gemm_nvfp4w_splits(int m, int n, int k, int splits);
  *   per device that loads the library, held until the process exits). The
  *   call allocates nothing.
  *   The first call on a device looks up that array's device address (once per
- *   device and CUDA context, with the device current); make that first call
- *   before any stream capture. A device reset destroys the context that holds
- *   the array: the next call looks the address up again, so after a reset the
- *   first call, too, should come before any capture. Every call shares the
+ *   device and CUDA context, with the device current). A device reset destroys
+ *   the context that holds the array: the next call looks the address up
+ *   again. Every call shares the
  *   array and it keeps the last call's contents; it needs no clearing, since
  *   the GEMM rewrites what the norm then reads. Calls that may run at the same
  *   time on the GPU (unordered streams) race on the array and give wrong

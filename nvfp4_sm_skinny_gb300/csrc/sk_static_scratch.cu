@@ -1,7 +1,6 @@
 // sk_gemm_rmsnorm_nvfp4_static: the pooler call (GEMM, pre-expert RMSNorm,
 // NVFP4) for callers that cannot allocate device memory, such as the enqueue
-// function of an inference-engine plugin that is handed no workspace, code
-// that records work into a CUDA graph (cudaMalloc is not capturable), or a
+// function of an inference-engine plugin that is handed no workspace, or a
 // serving loop whose device memory is budgeted once at start-up. The GEMM
 // output that the norm reads back lives in a fixed array in the library's
 // device image instead of a caller-provided workspace.

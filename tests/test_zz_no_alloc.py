@@ -1,6 +1,6 @@
 """sk_gemm_rmsnorm_nvfp4_static: the pooler call for callers that cannot
-allocate device memory (a plugin enqueue handed no workspace, work recorded
-into a CUDA graph, a serving loop with a fixed memory budget). Its GEMM output
+allocate device memory (a plugin enqueue handed no workspace, a serving loop
+with a fixed memory budget). Its GEMM output
 lives in the library's static device scratch instead of a workspace.
 
 Called here through the C ABI (ctypes) on two calls in a row with different
