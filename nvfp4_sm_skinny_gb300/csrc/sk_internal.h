@@ -32,15 +32,15 @@ constexpr int kMaxBoxesPerStage = 8;
 constexpr int kSlotXBytes = kTokTile * kBlockK * 2;  // 2 KiB
 constexpr int kMmaABytes = kMmaM * kBlockK * 2;      // 16 KiB read by one MMA row block
 constexpr int kMaxStages = 16;
-// MMA issue. One thread issuing tcgen05.mma is held for a fixed time per
-// instruction whatever its M and N (measured on GB300: ~75 ns), which at
-// 128 x 16 x 16 caps one issuer at ~55 GB/s of weight; the rate grows with the
-// number of issuing warps per SM. So a CTA issues from several warps: box j of
-// a stage goes to issuer j mod NI, and issuer q accumulates into its own TMEM
-// accumulator (16 FP32 columns), first written by the issuer's first box of
-// the slice (the issue cost, not the chained accumulation, sets the rate).
-// The epilogue adds the used accumulators in index order, so the sum order is
-// fixed.
+// MMA issue. One thread issuing tcgen05.mma is held ~144 ns per instruction
+// whatever its M (64, 128) and N (16 to 256); with four issuing warps an SM
+// reaches its floor of ~22 ns per 128 x 16 x 16 instruction, set by the
+// shared-memory reads of the operands (4.5 KiB per instruction, ~105 B per
+// clock), and more issuers do not lower it (measured on GB300). So a CTA
+// issues from four warps: box j of a stage goes to issuer j mod NI, and issuer
+// q accumulates into its own TMEM accumulator (16 FP32 columns), first written
+// by the issuer's first box of the slice. The epilogue adds the used
+// accumulators in index order, so the sum order is fixed.
 constexpr int kGemmIssuers = 4;
 constexpr int kNumAcc = kGemmIssuers;           // one per issuer
 constexpr int kTmemCols = 64;                   // kNumAcc * kTokTile, a power of two >= 32

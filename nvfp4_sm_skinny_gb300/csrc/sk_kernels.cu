@@ -395,11 +395,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // BF16 operand in tensor memory and put each block's activations in the
 // order of that operand, in two groups that take alternate blocks (one
 // group's barrier waits overlap the other's arithmetic); warps 0-3 run the
-// epilogue. Each MMA (128 weight rows x 16 tokens x 16) carries 2048 weights,
-// the same as in the BF16 GEMM, so the instruction count per SM is the same:
-// at 4.5 bits per weight the MMA issue rate of an SM (about one instruction
-// per 50 ns, whatever the number of issuing warps), not HBM, bounds this
-// kernel.
+// epilogue. At 4.5 bits per weight the expansion (about three instructions
+// per weight), not HBM and not the MMAs (an SM sustains one 128 x 16 x 16
+// instruction per ~18 ns with A in tensor memory), bounds this kernel.
 //
 // Expansion. Placing an e2m1 code's three magnitude bits at bits 6..8 of a
 // BF16 word and its sign at bit 15 gives the code's value times 2^-126
