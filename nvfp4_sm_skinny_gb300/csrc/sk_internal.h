@@ -33,18 +33,24 @@ constexpr int kSlotXBytes = kTokTile * kBlockK * 2;  // 2 KiB
 constexpr int kMmaABytes = kMmaM * kBlockK * 2;      // 16 KiB read by one MMA row block
 constexpr int kMaxStages = 16;
 // MMA issue. One thread issuing tcgen05.mma is held ~144 ns per instruction
-// whatever its M (64, 128) and N (16 to 256); with four issuing warps an SM
-// reaches its floor of ~22 ns per 128 x 16 x 16 instruction, set by the
-// shared-memory reads of the operands (4.5 KiB per instruction, ~105 B per
-// clock), and more issuers do not lower it (measured on GB300). So a CTA
-// issues from four warps: box j of a stage goes to issuer j mod NI, and issuer
-// q accumulates into its own TMEM accumulator (16 FP32 columns), first written
-// by the issuer's first box of the slice. The epilogue adds the used
-// accumulators in index order, so the sum order is fixed.
-constexpr int kGemmIssuers = 4;
-constexpr int kNumAcc = kGemmIssuers;           // one per issuer
-constexpr int kTmemCols = 64;                   // kNumAcc * kTokTile, a power of two >= 32
-static_assert(kNumAcc * kTokTile <= kTmemCols, "accumulators exceed the TMEM allocation");
+// whatever its M (64, 128) and N (16 to 256); an SM's floor is set by the
+// shared-memory reads of the operands (~105 B per clock: ~22 ns per
+// 128 x 16 x 16 instruction, 4.5 KiB, reached from four issuing warps; ~12 ns
+// per 64 x 16 x 16, 2.5 KiB, which takes about eight), measured on GB300. So
+// a CTA issues from NI warps (four for 128-row tiles, kGemmIssuers = eight
+// for tiles of at most 64 rows): box j of a stage goes to issuer j mod NI,
+// and issuer q accumulates into its own TMEM accumulator (16 FP32
+// columns), first written by the issuer's first box of the slice. The
+// epilogue adds the used accumulators in index order, so the sum order is
+// fixed. Tiles of at most 64 rows use the 64-row instruction (half the
+// operand reads); its accumulator row r sits in TMEM lane 32 * (r / 16) +
+// r % 16.
+constexpr int kGemmIssuers = 8;                 // the most issuing warps of a launch
+constexpr int kNumAcc = kGemmIssuers;           // one accumulator per issuer
+// The kernel is built for NI = 4 (128-row tiles) and NI = 8 (tiles of at most
+// 64 rows): 32 * (1 + NI) threads, NI * kTokTile TMEM columns.
+__host__ __device__ constexpr int gemm_issuers(int h) { return h <= 64 ? kGemmIssuers : kGemmIssuers / 2; }
+__host__ __device__ constexpr int gemm_threads(int ni) { return 32 * (1 + ni); }
 __host__ __device__ constexpr int acc_index(int q, int /*kk*/) { return q; }
 // Accumulators written by a K slice of nkb boxes moved bps per stage by ni
 // issuers: those of the issuers that own a box of the first stage.
@@ -141,7 +147,7 @@ size_t gemm_smem_bytes(int h, int stages, int bps, int splits);
 
 // Largest number of clusters of `splits` GEMM CTAs that can be resident at
 // once with `ctas_per_sm` (1 or 2) GEMM CTAs per SM (cached).
-int gemm_max_clusters(int device, int splits, int ctas_per_sm);
+int gemm_max_clusters(int device, int splits, int ctas_per_sm, int h = kMmaM);
 
 // The GEMM enqueued next, whose first weight stages a GEMM launch starts
 // towards L2 once it has issued its own last weight copy: its weight map (3-D,

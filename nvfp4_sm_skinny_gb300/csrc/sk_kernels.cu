@@ -24,10 +24,9 @@ __device__ uint32_t g_device_status;
 
 constexpr uint32_t kIdesc = idesc_bf16_f32(kMmaM, kTokTile);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s of wall time per wait
-// Warps 0-3 hold the 128 TMEM lanes in the epilogue (thread t = lane t);
-// warp 4 only issues MMAs.
-constexpr int kGemmThreads = 32 * (1 + kGemmIssuers);
-static_assert(kGemmThreads >= 128, "the epilogue needs four warps");
+// Warps 0-3 hold the 128 TMEM lanes in the epilogue; warps 4..NI only issue
+// MMAs.
+static_assert(gemm_threads(kGemmIssuers / 2) >= 128, "the epilogue needs four warps");
 
 struct GemmArgs {
   uint16_t *y;       // [m, n] BF16 bits
@@ -60,18 +59,19 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 }
 
 // Writes tile rows [r0, r1) of y (output features n0 + r0 ...; r1 - r0 and r0 a
-// multiple of 8): thread tid in [r0, r1) holds its row's 16 token values in v.
-// The values are staged as BF16 in shared memory, then each token's row
-// segment leaves in 16-byte stores (one per 8 features) instead of one 2-byte
-// store per token and feature. Called by all threads of the CTA.
+// multiple of 8): the thread whose `row` is in [r0, r1) holds that row's 16
+// token values in v (row < 0: none). The values are staged as BF16 in shared
+// memory, then each token's row segment leaves in 16-byte stores (one per 8
+// features) instead of one 2-byte store per token and feature. Called by all
+// threads of the CTA.
 template <int NT>
 __device__ __forceinline__ void store_tile_rows(uint16_t *stage, const float (&v)[kTokTile], int r0,
-                                                int r1, uint16_t *y, int n, int n0, int m,
-                                                bool ok) {
+                                                int r1, uint16_t *y, int n, int n0, int m, bool ok,
+                                                int row) {
   const int tid = threadIdx.x, nr = r1 - r0;
-  if (tid >= r0 && tid < r1) {
+  if (row >= r0 && row < r1) {
 #pragma unroll
-    for (int t = 0; t < kTokTile; ++t) stage[t * nr + (tid - r0)] = bf16_store_bits(v[t]);
+    for (int t = 0; t < kTokTile; ++t) stage[t * nr + (row - r0)] = bf16_store_bits(v[t]);
   }
   __syncthreads();
   const int per_t = nr >> 3;
@@ -87,9 +87,10 @@ __device__ __forceinline__ void store_tile_rows(uint16_t *stage, const float (&v
 // The GEMM epilogue after the accumulators are read: the split-K exchange
 // between the S ranks of the cluster (S > 1), the optional output scale, the
 // BF16 rounding (-0 stored as +0) and the stores of the tile's rows
-// [n0, n0 + h) of y (threads 0..h-1 hold one row each in acc). `stage` is
-// idle shared memory for the row staging, `red` the exchange buffer counted on
-// `red_bar`. Called by all NT threads of the CTA.
+// [n0, n0 + h) of y (each of rows 0..h-1 is held in acc by the one thread
+// whose `row` it is; row < 0: the thread holds none). `stage` is idle shared
+// memory for the row staging, `red` the exchange buffer counted on `red_bar`.
+// Called by all NT threads of the CTA.
 //
 // Split-K across the S ranks of the cluster: rank r owns tile rows
 // [r * R, (r + 1) * R). Every rank sends its FP32 partials of the rows it does
@@ -103,7 +104,7 @@ template <int NT, bool kScaled>
 __device__ __forceinline__ void splitk_store(const float (&acc)[kTokTile], float out_scale,
                                              uint16_t *stage, float *red, uint32_t red_bar,
                                              volatile uint32_t *abort_flag, bool aborted, int S,
-                                             int h, uint16_t *y, int n, int n0, int m) {
+                                             int h, uint16_t *y, int n, int n0, int m, int row) {
   const int tid = threadIdx.x;
   if (S == 1) {
     float v[kTokTile];
@@ -111,7 +112,7 @@ __device__ __forceinline__ void splitk_store(const float (&acc)[kTokTile], float
     for (int t = 0; t < kTokTile; ++t) v[t] = kScaled ? __fmul_rn(acc[t], out_scale) : acc[t];
     // Outputs may still be read or written by the previous kernel in the stream.
     griddep_wait();
-    store_tile_rows<NT>(stage, v, 0, h, y, n, n0, m, !aborted);
+    store_tile_rows<NT>(stage, v, 0, h, y, n, n0, m, !aborted, row);
     return;
   }
   const int R = (h + S - 1) / S;
@@ -122,10 +123,10 @@ __device__ __forceinline__ void splitk_store(const float (&acc)[kTokTile], float
   if (tid == 0)
     mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>((S - 1) * max(0, hi - lo) * ng * 16));
   cluster_wait();  // every peer's exchange barrier is initialised
-  if (tid < h) {
-    const uint32_t owner = static_cast<uint32_t>(tid / R);
+  if (row >= 0 && row < h) {
+    const uint32_t owner = static_cast<uint32_t>(row / R);
     if (owner != rank) {
-      const int lr = tid - static_cast<int>(owner) * R;
+      const int lr = row - static_cast<int>(owner) * R;
       const uint32_t dst =
           dsmem_map(smem_u32(red + (static_cast<int>(rank) * R + lr) * kTokTile), owner);
       const uint32_t rbar = dsmem_map(red_bar, owner);
@@ -137,14 +138,14 @@ __device__ __forceinline__ void splitk_store(const float (&acc)[kTokTile], float
     }
   }
   float v[kTokTile];
-  if (tid >= lo && tid < hi) {
+  if (row >= lo && row < hi) {
     if (!mbar_wait_bounded(red_bar, 0, kWaitLimitNs)) {
       atomicOr(&g_device_status, SK_DEVICE_WAIT_EPILOGUE);
       *abort_flag = 1;
     }
     // All sums first, then the stores: a load issued after a global store
     // that the compiler cannot prove disjoint waits behind it.
-    const int lr = tid - lo;
+    const int lr = row - lo;
 #pragma unroll
     for (int t = 0; t < kTokTile; ++t) v[t] = acc[t];
     if (rank != 0) {
@@ -185,11 +186,11 @@ __device__ __forceinline__ void splitk_store(const float (&acc)[kTokTile], float
   // stream (the exchange above stays within this cluster's shared memory).
   griddep_wait();
   if ((R & 7) == 0) {
-    store_tile_rows<NT>(stage, v, lo, hi > lo ? hi : lo, y, n, n0, m, ok);
-  } else if (ok && tid >= lo && tid < hi && n0 + tid < n) {
+    store_tile_rows<NT>(stage, v, lo, hi > lo ? hi : lo, y, n, n0, m, ok, row);
+  } else if (ok && row >= lo && row < hi && n0 + row < n) {
 #pragma unroll
     for (int t = 0; t < kTokTile; ++t)
-      if (t < m) y[static_cast<size_t>(t) * n + n0 + tid] = bf16_store_bits(v[t]);
+      if (t < m) y[static_cast<size_t>(t) * n + n0 + row] = bf16_store_bits(v[t]);
   }
 }
 
@@ -197,8 +198,9 @@ __device__ __forceinline__ void splitk_store(const float (&acc)[kTokTile], float
 // args.bps 64-column boxes per pipeline stage.
 // Warp 0 lane 0: TMA producer. Lane 0 of warps 1..kGemmIssuers: MMA issuers.
 // Warp 2 owns the TMEM allocation. Warps 0-3 run the epilogue (one TMEM lane
-// per thread).
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// per thread; with the 64-row instruction, lanes 0-15 of each warp).
+template <int NI>
+__global__ void __launch_bounds__(gemm_threads(NI), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_pf, GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -219,6 +221,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = args.h;
   const int n0 = blockIdx.x * h;
+  // Tiles of at most 64 rows: 64-row instructions, accumulator row r in TMEM
+  // lane 32 * (r / 16) + r % 16; otherwise row r in lane r.
+  const bool m64 = NI == kGemmIssuers && h <= 64;  // the launch pairs NI = 8 with h <= 64
+  const uint32_t idesc = idesc_bf16_f32(m64 ? 64 : kMmaM, kTokTile);
+  // Issuing warps: four reach the SM's floor for the 128-row instruction,
+  // the 64-row one needs eight (the launch picks NI by the tile height).
+  constexpr int ni = NI;
+  constexpr uint32_t kCols = NI * kTokTile;  // TMEM columns, a power of two >= 32
+  const int row = tid >= 128 ? -1 : !m64 ? tid : lane < 16 ? 16 * warp + lane : -1;
   const int nkb = args.kb_per_split;
   const int kb0 = blockIdx.y * nkb;
   const int nst = (nkb + B - 1) / B;                     // pipeline stages of work
@@ -232,9 +243,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kGemmIssuers);  // one commit per issuer
+      mbar_init(empty0 + 8 * s, ni);  // one commit per issuer
     }
-    mbar_init(done_bar, kGemmIssuers);
+    mbar_init(done_bar, ni);
     mbar_init(red_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -242,7 +253,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_map(&tmap_x);
   }
   if (warp == 2) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_alloc(smem_u32(tmem_slot), kCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
@@ -310,7 +321,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tma_prefetch_l2_3d(&tmap_pf, 0, pn0, pkb0 + j * args.pf_bps);
       }
     }
-  } else if (warp >= 1 && warp <= kGemmIssuers && lane == 0) {
+  } else if (warp >= 1 && warp <= ni && lane == 0) {
     // ---------------------------------------------------- MMA issuers
     const int q = warp - 1;
     bool started = false;  // this issuer's accumulators hold a partial sum
@@ -324,14 +335,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_after_sync();
       const int nb = min(B, nkb - i * B);
-      for (int j = q; j < nb; j += kGemmIssuers) {
+      for (int j = q; j < nb; j += ni) {
         const uint64_t adesc = smem_desc_k128(smem_u32(s_w + (s * B + j) * slot_w));
         const uint64_t bdesc = smem_desc_k128(smem_u32(s_x + (s * B + j) * kSlotXBytes));
 #pragma unroll
         for (int kk = 0; kk < kBlockK / 16; ++kk) {
           // K advances 16 elements = 32 bytes inside the 128-byte swizzle row.
           tc_mma_bf16(tmem + static_cast<uint32_t>(acc_index(q, kk) * kTokTile), adesc + 2 * kk,
-                      bdesc + 2 * kk, kIdesc, started || kk > 0);
+                      bdesc + 2 * kk, idesc, started || kk > 0);
         }
         started = true;
       }
@@ -362,11 +373,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
   for (int t = 0; t < kTokTile; ++t) acc[t] = 0.0f;
   if (warp < 4 && !aborted)
-    tmem_sum_accumulators<kNumAcc>(tmem + (static_cast<uint32_t>(warp * 32) << 16),
-                                   acc_used(nkb, B, kGemmIssuers), acc);
+    tmem_sum_accumulators<NI>(tmem + (static_cast<uint32_t>(warp * 32) << 16),
+                                   acc_used(nkb, B, ni), acc);
 
-  splitk_store<kGemmThreads, false>(acc, 1.0f, reinterpret_cast<uint16_t *>(s_w), red, red_bar,
-                                    abort_flag, aborted, S, h, args.y, args.n, n0, args.m);
+  splitk_store<gemm_threads(NI), false>(acc, 1.0f, reinterpret_cast<uint16_t *>(s_w), red, red_bar,
+                                    abort_flag, aborted, S, h, args.y, args.n, n0, args.m, row);
 
   tc_fence_before_sync();
   __syncthreads();
@@ -377,7 +388,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       atomicOr(&g_device_status, SK_DEVICE_WAIT_TEARDOWN);
     __syncwarp();
     tc_fence_after_sync();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, kCols);
   }
 }
 
@@ -701,7 +712,8 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   griddep_wait();
   const float out_scale = __fmul_rn(*args.w_scale, 128.0f);
   splitk_store<kW4Threads, true>(acc, out_scale, reinterpret_cast<uint16_t *>(s_q), red, red_bar,
-                                 abort_flag, aborted, S, kW4Rows, args.y, args.n, n0, args.m);
+                                 abort_flag, aborted, S, kW4Rows, args.y, args.n, n0, args.m,
+                                 tid < kW4Rows ? tid : -1);
 
   tc_fence_before_sync();
   __syncthreads();
@@ -1121,12 +1133,14 @@ cudaError_t device_setup(int device, DeviceInfo *info) {
     if (d.major == 10 && d.minor == 3) {
       // dynamic shared memory up to the opt-in limit less each kernel's static part
       cudaFuncAttributes fa;
-      if ((e = cudaFuncGetAttributes(&fa, gemm_kernel))) return e;
-      if ((e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(d.max_smem_optin - fa.sharedSizeBytes))))
-        return e;
-      if ((e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)))
-        return e;
+      for (auto *kern : {gemm_kernel<kGemmIssuers / 2>, gemm_kernel<kGemmIssuers>}) {
+        if ((e = cudaFuncGetAttributes(&fa, kern))) return e;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(d.max_smem_optin - fa.sharedSizeBytes))))
+          return e;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)))
+          return e;
+      }
       if ((e = cudaFuncGetAttributes(&fa, gemm_nvfp4w_kernel))) return e;
       if ((e = cudaFuncSetAttribute(gemm_nvfp4w_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(d.max_smem_optin - fa.sharedSizeBytes))))
@@ -1142,19 +1156,21 @@ cudaError_t device_setup(int device, DeviceInfo *info) {
   return cudaSuccess;
 }
 
-int gemm_max_clusters(int device, int splits, int ctas_per_sm) {
+int gemm_max_clusters(int device, int splits, int ctas_per_sm, int h) {
   static std::mutex mu;
-  static int cache[64][5][2];
+  static int cache[64][5][2][2];
   int idx = 0;
   while ((1 << idx) < splits && idx < 4) ++idx;
   const int per = ctas_per_sm >= 2 ? 1 : 0;
+  const int ni = gemm_issuers(h);
+  const int wide = ni == kGemmIssuers ? 1 : 0;
   if (device < 0 || device >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (cache[device][idx][per] == 0) {
+  if (cache[device][idx][per][wide] == 0) {
     int clusters = 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, splits, 1);
-    cfg.blockDim = dim3(kGemmThreads);
+    cfg.blockDim = dim3(gemm_threads(ni));
     // more than half an SM's shared memory: one CTA per SM; else two
     cfg.dynamicSmemBytes = per ? 100 * 1024 : 120 * 1024;
     cudaLaunchAttribute attr;
@@ -1164,11 +1180,12 @@ int gemm_max_clusters(int device, int splits, int ctas_per_sm) {
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_kernel, &cfg) != cudaSuccess || clusters < 1)
-      clusters = -1;
-    cache[device][idx][per] = clusters;
+    const cudaError_t oe = wide ? cudaOccupancyMaxActiveClusters(&clusters, gemm_kernel<kGemmIssuers>, &cfg)
+                                : cudaOccupancyMaxActiveClusters(&clusters, gemm_kernel<kGemmIssuers / 2>, &cfg);
+    if (oe != cudaSuccess || clusters < 1) clusters = -1;
+    cache[device][idx][per][wide] = clusters;
   }
-  return cache[device][idx][per];
+  return cache[device][idx][per][wide];
 }
 
 cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, uint16_t *y, int m,
@@ -1210,8 +1227,13 @@ cudaError_t launch_gemm(const CUtensorMap &tmap_w, const CUtensorMap &tmap_x, ui
     a.pf_ctas = pf->tiles * pf->splits;
   }
   const dim3 grid((n + h - 1) / h, splits, 1);
-  return launch_ex(gemm_kernel, grid, dim3(kGemmThreads), gemm_smem_bytes(h, stages, bps, splits), stream, pdl,
-                   dim3(1, splits, 1), tmap_w, tmap_x, a.pf_stages ? pf->map : tmap_w, a);
+  const size_t smem = gemm_smem_bytes(h, stages, bps, splits);
+  const CUtensorMap &tmap_pf = a.pf_stages ? pf->map : tmap_w;
+  if (gemm_issuers(h) == kGemmIssuers)
+    return launch_ex(gemm_kernel<kGemmIssuers>, grid, dim3(gemm_threads(kGemmIssuers)), smem, stream,
+                     pdl, dim3(1, splits, 1), tmap_w, tmap_x, tmap_pf, a);
+  return launch_ex(gemm_kernel<kGemmIssuers / 2>, grid, dim3(gemm_threads(kGemmIssuers / 2)), smem,
+                   stream, pdl, dim3(1, splits, 1), tmap_w, tmap_x, tmap_pf, a);
 }
 
 // Cluster size and CTA width of a norm over `units` per row (NVFP4 blocks or
