@@ -475,16 +475,18 @@ __device__ __forceinline__ uint32_t w4_scale_pair(uint32_t sf) {
 
 // The four BF16 pairs (W[j], W[j + 4]), j = 0..3, of 8 codes (code j in bits
 // 4j..4j+3) times the scale pair c2, each an exact code * scale * 2^-7. Codes
-// j and j + 4 sit 16 bits apart, so one left shift places both magnitudes at
-// bits 6..8 / 22..24 and another both signs at bits 15 / 31; the shifts are
-// written as multiplies (they run on the multiply-add pipe, beside the
-// logic operations), codes 2, 3, 6, 7 after one right shift of the word.
+// j and j + 4 sit 16 bits apart. Masking one such pair of nibbles and
+// multiplying by 2^6 + 2^12 (2^2 + 2^8 for the odd nibbles) makes two copies
+// of each nibble in disjoint bit ranges, one shifted so that its magnitude
+// bits land at 6..8 and one so that its sign lands at 15; a second mask keeps
+// just those. Codes 2, 3, 6, 7 go the same way after one right shift of the
+// word.
 __device__ __forceinline__ void w4_expand8(uint32_t w, uint32_t c2, uint32_t *o) {
   const uint32_t h = w >> 8;
-  o[0] = mul_bf16x2(((w * 64u) & 0x01C001C0u) | ((w * 4096u) & 0x80008000u), c2);
-  o[1] = mul_bf16x2(((w * 4u) & 0x01C001C0u) | ((w * 256u) & 0x80008000u), c2);
-  o[2] = mul_bf16x2(((h * 64u) & 0x01C001C0u) | ((h * 4096u) & 0x80008000u), c2);
-  o[3] = mul_bf16x2(((h * 4u) & 0x01C001C0u) | ((h * 256u) & 0x80008000u), c2);
+  o[0] = mul_bf16x2(((w & 0x000F000Fu) * 4160u) & 0x81C081C0u, c2);
+  o[1] = mul_bf16x2(((w & 0x00F000F0u) * 260u) & 0x81C081C0u, c2);
+  o[2] = mul_bf16x2(((h & 0x000F000Fu) * 4160u) & 0x81C081C0u, c2);
+  o[3] = mul_bf16x2(((h & 0x00F000F0u) * 260u) & 0x81C081C0u, c2);
 }
 
 __global__ void __launch_bounds__(kW4Threads, 1)
