@@ -1311,9 +1311,13 @@ cudaError_t launch_rmsnorm_nvfp4(const uint16_t *y, const uint16_t *norm_w, floa
                                  const float *gs, uint8_t *a, uint8_t *a_sf, uint16_t *z_out,
                                  int m, int n, cudaStream_t stream, bool pdl) {
   // one thread per 16-column block, a cluster of CTAs per token row
-  // (n <= 16384: at most 1024 blocks over at most 8 CTAs)
+  // (n <= 16384: at most 1024 blocks over at most 8 CTAs), at least 64 blocks
+  // per CTA: at n = 4096, 4 CTAs of 64 threads (measured on GB300 against 8
+  // of 32: the pooler call 13.8 against 14.6 us at b = 8, the decode chain
+  // 0.03 us per layer faster; the wait for the cluster's slowest CTA is
+  // shorter with fewer of them)
   int C, threads;
-  norm_shape(n / 16, 32, &C, &threads);
+  norm_shape(n / 16, 64, &C, &threads);
   return launch_ex(rmsnorm_nvfp4_kernel, dim3(C, m), dim3(threads), 0, stream, pdl, dim3(C, 1, 1),
                    y, norm_w, eps, gc, gs, a, a_sf, z_out, n, C);
 }
