@@ -68,6 +68,24 @@ def test_one_hot_power_of_two_weight_is_exact(sk):
         assert np.array_equal(y, synth.bits(want)), splits
 
 
+@pytest.mark.parametrize("n,k", [(1024, 4096), (8192, 1024), (4096, 8192)])
+def test_one_hot_weight_exact_on_auto_plans(sk, n, k):
+    # The automatic plans of these shapes use 64-row tiles with split 4, 56-row
+    # tiles (both with the 64-row MMA, whose accumulator rows sit in lanes
+    # 32 * (r / 16) + r % 16) and 128-row tiles with split 4: with one
+    # power-of-two weight per row every output is a single exact product, so
+    # a row read from the wrong TMEM lane or stored to the wrong feature shows.
+    g = torch.Generator().manual_seed(n + k)
+    perm = torch.randint(0, k, (n,), generator=g)
+    scale = 2.0 ** torch.randint(-3, 4, (n,), generator=g).float()
+    w = torch.zeros(n, k, dtype=torch.bfloat16)
+    w[torch.arange(n), perm] = scale.to(torch.bfloat16)
+    x = synth.normal_bf16((16, k), 1.0, 9)
+    y = run(sk, x, w, 0)
+    want = (x.float()[:, perm] * scale[None]).to(torch.bfloat16)
+    assert np.array_equal(y, synth.bits(want))
+
+
 def test_zero_activations_give_positive_zero(sk):
     w = synth.normal_bf16((256, 512), 0.02, 5)
     for xval in (0.0, -0.0):
