@@ -196,7 +196,7 @@ __device__ __forceinline__ void splitk_store(const float (&acc)[kTokTile], float
 
 // One CTA = h weight rows x one K slice of kb_per_split * 64 elements, moved
 // args.bps 64-column boxes per pipeline stage.
-// Warp 0 lane 0: TMA producer. Lane 0 of warps 1..kGemmIssuers: MMA issuers.
+// Warp 0 lane 0: TMA producer. Lane 0 of warps 1..NI: MMA issuers.
 // Warp 2 owns the TMEM allocation. Warps 0-3 run the epilogue (one TMEM lane
 // per thread; with the 64-row instruction, lanes 0-15 of each warp).
 template <int NI>
