@@ -577,35 +577,57 @@ def run_gpu(args, world, rank, local):
     pin = dict(pin_memory=True)
     h_host = h0.cpu().pin_memory()
     s_host = s0.cpu().pin_memory()
-    # two sets of pinned result buffers: step i's results are read on the host
-    # while step i + 1 runs
+    # Two buffer sets on the same weights, one graph each, so that step i + 1's
+    # inputs are copied in and step i - 1's results copied out while step i
+    # runs, as a serving loop overlaps its I/O with compute; each set has its
+    # own pinned result buffers, read on the host while the next step runs.
+    chain_b = chain.twin()
+    chain_b.set_input(h0, s0)
+    g_chain_b = chain_b.capture(chain_b.forward)
+    sets = [(chain, g_chain), (chain_b, g_chain_b)]
     outs = [(torch.empty(M_ROWS, synth.HIDDEN, dtype=torch.bfloat16, **pin),
              torch.empty(M_ROWS, synth.POOLED // 2, dtype=torch.uint8, **pin),
              torch.empty(M_ROWS, synth.POOLED // 16, dtype=torch.uint8, **pin)) for _ in range(2)]
     h2d = h_host.numel() * 2 + s_host.numel() * 4
     d2h = sum(t.numel() * t.element_size() for t in outs[0])
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
 
     def e2e_steps_run(n_steps):
-        """n_steps decode steps as a serving loop runs them: each step copies its
-        inputs in, replays the chain and copies its results out (one stream,
-        so in order); the host queues step i + 1 before it waits for step i's
-        results."""
-        done = None
+        """n_steps decode steps as a pipelined serving loop runs them. Step i
+        uses buffer set i % 2: its inputs are copied in on s_in once step
+        i - 2's graph and result copies on that set are done, its graph runs on
+        the compute stream once they have landed, and its results are copied
+        out on s_out once it has run. The host queues step i + 1 before it
+        waits for step i's results."""
+        out_done = [None, None]
         for i in range(n_steps):
-            out_h, out_a, out_sf = outs[i % 2]
+            k = i % 2
+            c, g = sets[k]
+            out_h, out_a, out_sf = outs[k]
+            with torch.cuda.stream(s_in):
+                if out_done[k] is not None:
+                    s_in.wait_event(out_done[k])
+                c.h[0].copy_(h_host, non_blocking=True)
+                c.s.copy_(s_host, non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
             with torch.cuda.stream(stream):
-                chain.h[0].copy_(h_host, non_blocking=True)
-                chain.s.copy_(s_host, non_blocking=True)
-                g_chain.replay()
-                out_h.copy_(chain.h[L], non_blocking=True)
-                out_a.copy_(chain.a[L - 1], non_blocking=True)
-                out_sf.copy_(chain.a_sf[L - 1], non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(stream)
-            if done is not None:
-                done.synchronize()  # step i - 1's results are on the host
-            done = ev
-        done.synchronize()
+                stream.wait_event(ev_in)
+                g.replay()
+                ev_g = torch.cuda.Event()
+                ev_g.record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_g)
+                out_h.copy_(c.h[L], non_blocking=True)
+                out_a.copy_(c.a[L - 1], non_blocking=True)
+                out_sf.copy_(c.a_sf[L - 1], non_blocking=True)
+                ev_o = torch.cuda.Event()
+                ev_o.record(s_out)
+            out_done[k] = ev_o
+            if i >= 1:
+                out_done[(i - 1) % 2].synchronize()  # step i - 1's results are on the host
+        out_done[(n_steps - 1) % 2].synchronize()
 
     e2e_steps_run(3)
     e2e_steps = max(10, min(args.steps, 300))
@@ -615,6 +637,10 @@ def run_gpu(args, world, rank, local):
     e2e_steps_run(e2e_steps)
     t_e2e = reduce_max(time.perf_counter() - t0, dist, dev)
     e2e_value = aggregate_rate(bytes_step, e2e_steps, world, t_e2e)
+    # both buffer sets ran the same inputs: their results must agree bit for bit
+    if not all(torch.equal(a.view(torch.uint8), b.view(torch.uint8)) for a, b in zip(*outs)):
+        raise RuntimeError("the two buffer sets of the end-to-end loop disagree")
+    del g_chain_b, chain_b
     status = sk.device_status()
 
     per_config = None

@@ -16,6 +16,8 @@ CUDA graph (the calls allocate nothing and are capturable).
 """
 from __future__ import annotations
 
+import copy
+
 import torch
 
 import nvfp4_sm_skinny_gb300 as sk
@@ -75,6 +77,15 @@ class DecodeChain:
         self.ws_o = torch.zeros(layers, sk.gemm_dual_norm_workspace(m, H), dtype=torch.uint8, device=dev)
         self.ws_p = torch.zeros(layers, sk.gemm_rmsnorm_nvfp4_workspace(m, P), dtype=torch.uint8,
                                 device=dev)
+
+    def twin(self) -> "DecodeChain":
+        """A chain on the same weights and global scales with its own
+        activation buffers and workspaces, so that two steps can be in flight
+        (one copying its inputs in or results out while the other runs)."""
+        t = copy.copy(self)
+        for name in ("h", "s", "u", "z", "a", "a_sf", "ws_o", "ws_p"):
+            setattr(t, name, torch.zeros_like(getattr(self, name)))
+        return t
 
     def set_input(self, h0: torch.Tensor, s0: torch.Tensor) -> None:
         self.h[0].copy_(h0)
